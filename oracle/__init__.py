@@ -1,0 +1,17 @@
+"""Float64 CPU oracle for exact softmax attention (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` use this package.  The CUDA library never imports it.
+"""
+
+from .attention import (  # noqa: F401
+    attention_backward,
+    attention_forward,
+    attention_probs,
+    attention_rows,
+    backward_delta,
+    merge_partials,
+    online_attention,
+    scores,
+    split_partials,
+)

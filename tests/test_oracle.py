@@ -1,0 +1,270 @@
+"""Pins for the float64 oracle (CPU only).
+
+Each test ties the oracle to something outside itself: the worked example the
+lesson prints ("FlashAttention：IO-aware 的注意力 kernel", §4), closed forms,
+invariants of softmax attention, scipy's softmax / logsumexp, brute force on
+tiny inputs and central finite differences for the backward.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import special
+
+import oracle
+
+RNG = np.random.default_rng(1234)
+
+
+def _worked(golden_dir):
+    with open(os.path.join(golden_dir, "worked_example.json")) as f:
+        g = json.load(f)
+    q = np.array(g["q"])[None, :]
+    K = np.array(g["K"])
+    V = np.array(g["V"])
+    return g, q, K, V, 1.0 / math.sqrt(q.shape[1])
+
+
+def test_worked_example_matches_printed_output(golden_dir):
+    g, q, K, V, scale = _worked(golden_dir)
+    o, lse = oracle.attention_forward(q, K, V, scale)
+    assert np.all(np.round(o[0], g["O_decimals"]) == np.array(g["O_printed"]))
+    # The printed values are rounded to 6 decimals.
+    assert np.max(np.abs(o[0] - np.array(g["O_printed"]))) <= 5e-7
+    assert np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("block", [1, 2, 3, 6])
+def test_worked_example_online_equals_full(golden_dir, block):
+    g, q, K, V, scale = _worked(golden_dir)
+    o_full, lse_full = oracle.attention_forward(q, K, V, scale)
+    o_on, lse_on = oracle.online_attention(q, K, V, scale, block)
+    # The lesson prints 1.11e-16 for block=2: floating point noise, not error.
+    assert np.max(np.abs(o_full - o_on)) <= 4 * np.finfo(np.float64).eps
+    assert np.max(np.abs(lse_full - lse_on)) <= 8 * np.finfo(np.float64).eps
+    assert np.all(np.round(o_on[0], 6) == np.array(g["O_printed"]))
+
+
+def test_worked_example_by_brute_force(golden_dir):
+    """Independent scalar evaluation with math.fsum on the printed example."""
+    g, q, K, V, scale = _worked(golden_dir)
+    s = [math.fsum(a * b for a, b in zip(q[0], k)) / 2.0 for k in K]   # sqrt(4) = 2
+    z = math.fsum(math.exp(x) for x in s)
+    o = [math.fsum(math.exp(s[i]) / z * V[i][t] for i in range(len(K))) for t in range(4)]
+    lse = math.log(z)
+    o_ref, lse_ref = oracle.attention_forward(q, K, V, scale)
+    assert np.max(np.abs(np.array(o) - o_ref[0])) < 1e-15
+    assert abs(lse - lse_ref[0]) < 1e-15
+
+
+@pytest.mark.parametrize("nq,nk,d", [(5, 7, 3), (16, 33, 8), (1, 1, 4)])
+def test_matches_scipy_softmax_and_logsumexp(nq, nk, d):
+    q = RNG.standard_normal((nq, d))
+    k = RNG.standard_normal((nk, d))
+    v = RNG.standard_normal((nk, d))
+    scale = 1.0 / math.sqrt(d)
+    s = np.einsum("it,jt->ij", q, k) * scale
+    o, lse = oracle.attention_forward(q, k, v, scale)
+    assert np.allclose(o, special.softmax(s, axis=1) @ v, rtol=0, atol=1e-13)
+    assert np.allclose(lse, special.logsumexp(s, axis=1), rtol=0, atol=1e-13)
+
+
+def test_values_all_ones_give_all_ones():
+    q = RNG.standard_normal((9, 6))
+    k = RNG.standard_normal((13, 6))
+    o, _ = oracle.attention_forward(q, k, np.ones((13, 6)), 0.4)
+    assert np.allclose(o, 1.0, atol=1e-14)
+
+
+def test_identity_values_give_probabilities_with_unit_row_sums():
+    n = 11
+    q = RNG.standard_normal((7, n))
+    k = RNG.standard_normal((n, n))
+    o, _ = oracle.attention_forward(q, k, np.eye(n), 0.3)
+    p = oracle.attention_probs(q, k, 0.3)
+    assert np.allclose(o, p, atol=1e-15)
+    assert np.allclose(p.sum(axis=1), 1.0, atol=1e-12)
+    assert (p > 0).all()
+
+
+def test_shift_of_all_keys_shifts_lse_not_output():
+    q = RNG.standard_normal((8, 5))
+    k = RNG.standard_normal((10, 5))
+    v = RNG.standard_normal((10, 5))
+    w = RNG.standard_normal(5) * 3
+    scale = 0.7
+    o0, l0 = oracle.attention_forward(q, k, v, scale)
+    o1, l1 = oracle.attention_forward(q, k + w, v, scale)
+    assert np.allclose(o0, o1, atol=1e-12)
+    assert np.allclose(l1 - l0, scale * (q @ w), atol=1e-12)
+
+
+def test_equal_keys_give_uniform_weights():
+    n, d = 12, 4
+    q = RNG.standard_normal((3, d))
+    k = np.tile(RNG.standard_normal((1, d)), (n, 1))
+    v = RNG.standard_normal((n, d))
+    o, lse = oracle.attention_forward(q, k, v, 0.5)
+    assert np.allclose(o, v.mean(axis=0)[None, :], atol=1e-14)
+    assert np.allclose(lse, 0.5 * (q @ k[0]) + math.log(n), atol=1e-13)
+
+
+def test_single_key_returns_its_value_and_score():
+    q = RNG.standard_normal((4, 3))
+    k = RNG.standard_normal((1, 3))
+    v = RNG.standard_normal((1, 3))
+    o, lse = oracle.attention_forward(q, k, v, 1.3)
+    assert np.allclose(o, np.tile(v, (4, 1)), atol=1e-15)
+    assert np.allclose(lse, 1.3 * (q @ k[0]), atol=1e-15)
+
+
+def test_large_scores_are_stable():
+    q = RNG.standard_normal((4, 8)) * 40
+    k = RNG.standard_normal((20, 8)) * 40
+    v = RNG.standard_normal((20, 8))
+    o, lse = oracle.attention_forward(q, k, v, 1.0)
+    s = q @ k.T
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert np.allclose(lse, special.logsumexp(s, axis=1), rtol=1e-15, atol=1e-12)
+
+
+def test_permutation_equivariance():
+    q = RNG.standard_normal((6, 4))
+    k = RNG.standard_normal((9, 4))
+    v = RNG.standard_normal((9, 4))
+    pk = RNG.permutation(9)
+    pq = RNG.permutation(6)
+    o, lse = oracle.attention_forward(q, k, v, 0.5)
+    o2, lse2 = oracle.attention_forward(q[pq], k[pk], v[pk], 0.5)
+    assert np.allclose(o[pq], o2, atol=1e-14)
+    assert np.allclose(lse[pq], lse2, atol=1e-14)
+
+
+def test_row_block_does_not_change_result():
+    q = RNG.standard_normal((2, 3, 37, 8))
+    k = RNG.standard_normal((2, 3, 29, 8))
+    v = RNG.standard_normal((2, 3, 29, 8))
+    ref = oracle.attention_forward(q, k, v, 0.35, row_block=None)
+    for rb in (1, 7, 16, 256):
+        o, lse = oracle.attention_forward(q, k, v, 0.35, row_block=rb)
+        assert np.max(np.abs(o - ref[0])) <= 1e-12
+        assert np.max(np.abs(lse - ref[1])) <= 1e-12
+
+
+def test_rows_helper_matches_full():
+    q = RNG.standard_normal((40, 8))
+    k = RNG.standard_normal((50, 8))
+    v = RNG.standard_normal((50, 8))
+    o, lse = oracle.attention_forward(q, k, v, 0.3)
+    rows = [0, 5, 39, 17]
+    o2, lse2 = oracle.attention_rows(q, k, v, 0.3, rows)
+    assert np.max(np.abs(o2 - o[rows])) <= 1e-14
+    assert np.max(np.abs(lse2 - lse[rows])) <= 1e-14
+
+
+@pytest.mark.parametrize("block", [1, 5, 16, 64])
+def test_online_matches_definition_random(block):
+    q = RNG.standard_normal((12, 16))
+    k = RNG.standard_normal((61, 16)) * 2
+    v = RNG.standard_normal((61, 16))
+    o, lse = oracle.attention_forward(q, k, v, 0.25)
+    o2, lse2 = oracle.online_attention(q, k, v, 0.25, block)
+    assert np.max(np.abs(o - o2)) <= 1e-13
+    assert np.max(np.abs(lse - lse2)) <= 1e-13
+
+
+@pytest.mark.parametrize("nk,n_splits", [(256, 32), (100, 32), (8, 32), (1000, 7), (5, 1)])
+def test_split_merge_equals_full_row(nk, n_splits):
+    q = RNG.standard_normal((1, 16))
+    k = RNG.standard_normal((nk, 16))
+    v = RNG.standard_normal((nk, 16))
+    o, lse = oracle.attention_forward(q, k, v, 0.25)
+    ms, ls, os_ = oracle.split_partials(q, k, v, 0.25, n_splits)
+    o2, lse2 = oracle.merge_partials(ms, ls, os_)
+    assert np.max(np.abs(o - o2)) <= 1e-13
+    assert np.max(np.abs(lse - lse2)) <= 1e-13
+
+
+def test_merge_of_two_single_key_chunks_closed_form():
+    # Chunk a holds one key with score sa, chunk b one key with score sb:
+    # the merged result is the two-key softmax, worked out by hand.
+    sa, sb = 0.3, -1.1
+    va, vb = np.array([[1.0, 2.0]]), np.array([[-3.0, 0.5]])
+    ms = np.array([[sa], [sb]])
+    ls = np.array([[1.0], [1.0]])
+    os_ = np.stack([va, vb])
+    o, lse = oracle.merge_partials(ms, ls, os_)
+    wa = 1.0 / (1.0 + math.exp(sb - sa))
+    assert np.allclose(o[0], wa * va[0] + (1 - wa) * vb[0], atol=1e-15)
+    assert abs(lse[0] - (sa + math.log1p(math.exp(sb - sa)))) < 1e-15
+
+
+# ---------------------------------------------------------------- backward
+
+
+def _loss(q, k, v, do, scale):
+    o, _ = oracle.attention_forward(q, k, v, scale)
+    return float(np.sum(o * do))
+
+
+@pytest.mark.parametrize("n,nk,d", [(4, 4, 3), (6, 8, 4), (1, 5, 2)])
+def test_backward_matches_finite_differences(n, nk, d):
+    rng = np.random.default_rng(n * 100 + nk * 10 + d)
+    q = rng.standard_normal((n, d))
+    k = rng.standard_normal((nk, d))
+    v = rng.standard_normal((nk, d))
+    do = rng.standard_normal((n, d))
+    scale = 1.0 / math.sqrt(d)
+    if n == nk:
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, scale)
+    else:
+        # The library's backward is square (self-attention); the oracle's
+        # per-head gradient is general, exercise it directly.
+        from oracle.attention import _head_backward
+        dq, dk, dv, _ = _head_backward(q, k, v, do, scale)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp = x.copy()
+            xm = x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = {"q": q, "k": k, "v": v}
+            args_p[name] = xp
+            args_m[name] = xm
+            num[idx] = (_loss(args_p["q"], args_p["k"], args_p["v"], do, scale)
+                        - _loss(args_m["q"], args_m["k"], args_m["v"], do, scale)) / (2 * h)
+        err = np.linalg.norm(num - g) / max(np.linalg.norm(num), 1e-30)
+        assert err <= 1e-6, (name, err)
+
+
+def test_backward_delta_identity():
+    q = RNG.standard_normal((10, 6))
+    k = RNG.standard_normal((10, 6))
+    v = RNG.standard_normal((10, 6))
+    do = RNG.standard_normal((10, 6))
+    p = oracle.attention_probs(q, k, 0.4)
+    o, _ = oracle.attention_forward(q, k, v, 0.4)
+    dp = do @ v.T
+    assert np.allclose(np.sum(p * dp, axis=1), oracle.backward_delta(do, o), atol=1e-13)
+
+
+def test_backward_matches_torch_autograd_fp64():
+    torch = pytest.importorskip("torch")
+    q = RNG.standard_normal((2, 3, 17, 8))
+    k = RNG.standard_normal((2, 3, 17, 8))
+    v = RNG.standard_normal((2, 3, 17, 8))
+    do = RNG.standard_normal((2, 3, 17, 8))
+    scale = 0.3
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, scale)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    o = torch.softmax(scale * tq @ tk.transpose(-1, -2), dim=-1) @ tv
+    o.backward(torch.tensor(do))
+    assert np.allclose(tq.grad.numpy(), dq, atol=1e-12)
+    assert np.allclose(tk.grad.numpy(), dk, atol=1e-12)
+    assert np.allclose(tv.grad.numpy(), dv, atol=1e-12)
