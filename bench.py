@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark: exact attention on one GB300 through the libfa C ABI.
+
+Headline (one JSON line): forward prefill at B=4, H=32, N=4096, d=128 bf16,
+no mask, reported as attention TFLOP/s = 4·B·H·N²·d / time.  The same line
+carries, measured in the same process: the long-context forward
+(B=1, H=32, N=32768), split-KV decode (B=64, H=32, N_kv=8192, 32 splits,
+HBM GB/s and tokens/s) and the training forward + backward (B=2, H=16,
+N=8192), each with its fraction of the roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas: (b, h) pairs are independent, there is no exchange
+step); rank 0 prints the line with value = all ranks' work / slowest rank.
+``--impl reference`` times the float64 CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (4·B·H·N²·d) and % of GB300 BF16 peak; decode HBM GB/s"
+UNIT = "TFLOP/s"
+PREFILL = dict(B=4, H=32, N=4096, d=128)
+LONG = dict(B=1, H=32, N=32768, d=128)
+DECODE = dict(B=64, H=32, N=8192, d=128, splits=32)
+TRAIN = dict(B=2, H=16, N=8192, d=128)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch from one ncu capture of each kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the sha256 of the kernel's sources at capture
+# time; a changed kernel reports null until it is captured again.
+NCU_TRAFFIC = {}
+
+
+def fwd_flops(B, H, N, d, Nkv=None):
+    return 4.0 * B * H * N * (N if Nkv is None else Nkv) * d
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "io_aware_exact_11_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, srcs):
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec and rec["src"] == source_hash(*srcs):
+        return rec["bytes"]
+    return None
+
+
+# ------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity for one rank)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.sel = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            self.sel = vis.split(",")[device_index] if vis else str(device_index)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in self.samples if num(s[1]) is not None]
+        mx = [num(s[2]) for s in self.samples if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower().startswith("active")})
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------- CPU oracle
+_HEAD = {}
+
+
+def oracle_sample(budget_s: float, min_blocks: int = 1):
+    """The float64 oracle on rows of one prefill head, until ~budget_s elapsed."""
+    import numpy as np
+    import oracle
+    from io_aware_exact_11_gb300 import inputs
+
+    N, d = PREFILL["N"], PREFILL["d"]
+    if not _HEAD:
+        _HEAD.update({n: inputs.head_as_f64(1, n, 0, 0, N, d) for n in ("q", "k", "v")})
+    q, k, v = _HEAD["q"], _HEAD["k"], _HEAD["v"]
+    scale = 1 / math.sqrt(d)
+    rows_done = 0
+    block = 256
+    t0 = time.perf_counter()
+    while True:
+        r0 = rows_done % N
+        oracle.attention_rows(q, k, v, scale, np.arange(r0, min(N, r0 + block)))
+        rows_done += min(block, N - r0)
+        el = time.perf_counter() - t0
+        if rows_done >= min_blocks * block and el >= budget_s:
+            break
+    flops = 4.0 * rows_done * N * d
+    return flops / el / 1e12, rows_done, el
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, ws, rank):
+    """The oracle as the reference arm: host cores, bounded sample per step."""
+    if rank != 0:
+        return
+    # Keep the whole run to about two minutes whatever --steps/--warmup are.
+    per_step = max(0.05, min(2.0, 120.0 / (args.steps + args.warmup / 4)))
+    oracle_sample(0.5)  # warm BLAS threads
+    for _ in range(args.warmup):
+        oracle_sample(per_step / 4)
+    vals, rows, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        v, r, s = oracle_sample(per_step)
+        vals.append(v)
+        rows += r
+        secs += s
+    value = 4.0 * rows * PREFILL["N"] * PREFILL["d"] / secs / 1e12
+    sample = (f"float64 oracle on query rows of one prefill head (N=4096, d=128), "
+              f"{rows} rows over {args.steps} steps of ~{per_step:.2f} s")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill forward B=4 H=32 N=4096 d=128 (bounded row sample)", "parallelism": "host"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, ws, rank, local):
+    import torch
+    from io_aware_exact_11_gb300 import fa
+
+    if not os.path.exists(fa.LIB_PATH):
+        from io_aware_exact_11_gb300 import build
+        build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev)
+
+    def randn(shape, seed):
+        gen.manual_seed(seed * 1000003 + rank)
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return e0.elapsed_time(e1) / 1e3
+
+    # ---------------- headline: prefill forward
+    B, H, N, d = PREFILL["B"], PREFILL["H"], PREFILL["N"], PREFILL["d"]
+    q, k, v = randn((B, H, N, d), 1), randn((B, H, N, d), 2), randn((B, H, N, d), 3)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def step():
+        fa.forward(q, k, v, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    fa.device_status()
+    launches0 = fa.launch_count()
+    with ClockSampler(local) as clk:
+        el = timed(step, args.steps, 0)
+    launches = fa.launch_count() - launches0
+    fa.device_status()
+    el_max = max_over_ranks(el, ws, dev)
+    flops = fwd_flops(B, H, N, d)
+    value = flops * args.steps * ws / el_max / 1e12
+    per_launch = el / args.steps
+    achieved = flops / per_launch / 1e12
+    peak = float(peaks["bf16_tflops"])
+
+    # ---------------- e2e: host buffers, copies inside the timed region
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        fa.forward(q, k, v, out=o, lse=lse)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    el_e2e = max_over_ranks(timed(e2e_step, e2e_steps, 2), ws, dev)
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * 4
+    e2e_value = flops * e2e_steps * ws / el_e2e / 1e12
+    del qh, kh, vh, oh, lh
+
+    extra = {}
+    if not args.quick:
+        # ---------------- long-context forward
+        Bl, Hl, Nl = LONG["B"], LONG["H"], LONG["N"]
+        del q, k, v, o, lse
+        ql, kl, vl = randn((Bl, Hl, Nl, d), 4), randn((Bl, Hl, Nl, d), 5), randn((Bl, Hl, Nl, d), 6)
+        ol = torch.empty_like(ql)
+        ll = torch.empty((Bl, Hl, Nl), dtype=torch.float32, device=dev)
+        n_long = max(2, min(args.steps // 10, 10))
+        t_long = timed(lambda: fa.forward(ql, kl, vl, out=ol, lse=ll), n_long, 1) / n_long
+        fl = fwd_flops(Bl, Hl, Nl, d)
+        extra["long_forward"] = {"workload": "B=1 H=32 N=32768 d=128 bf16", "tflops": fl / t_long / 1e12,
+                                 "ms": t_long * 1e3, "frac_of_bf16_peak": fl / t_long / 1e12 / peak}
+        del ql, kl, vl, ol, ll
+
+        # ---------------- decode
+        Bd, Hd, Nd, S = DECODE["B"], DECODE["H"], DECODE["N"], DECODE["splits"]
+        qd = randn((Bd, Hd, 1, d), 7)
+        kd, vd = randn((Bd, Hd, Nd, d), 8), randn((Bd, Hd, Nd, d), 9)
+        od = torch.empty_like(qd)
+        ld = torch.empty((Bd, Hd), dtype=torch.float32, device=dev)
+        ws_d = torch.empty(fa.decode_workspace_size(Bd, Hd, d, S), dtype=torch.uint8, device=dev)
+        n_dec = max(5, min(args.steps, 50))
+        t_dec = timed(lambda: fa.decode_splitkv(qd, kd, vd, n_splits=S, out=od, lse=ld, workspace=ws_d),
+                      n_dec, 2) / n_dec
+        kv_bytes = 2.0 * Bd * Hd * Nd * d * 2
+        extra["decode"] = {"workload": "B=64 H=32 S_q=1 N_kv=8192 d=128 bf16, 32 splits",
+                           "hbm_gbs": kv_bytes / t_dec / 1e9, "tokens_per_s": Bd / t_dec, "ms": t_dec * 1e3,
+                           "frac_of_hbm_peak": kv_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"]),
+                           "bytes_per_step": kv_bytes}
+        del qd, kd, vd, od, ld, ws_d
+
+        # ---------------- training forward + backward
+        Bt, Ht, Nt = TRAIN["B"], TRAIN["H"], TRAIN["N"]
+        qt, kt, vt, dot = (randn((Bt, Ht, Nt, d), s) for s in (10, 11, 12, 13))
+        ot = torch.empty_like(qt)
+        lt = torch.empty((Bt, Ht, Nt), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(qt), torch.empty_like(kt), torch.empty_like(vt)
+        ws_b = torch.empty(fa.backward_workspace_size(Bt, Ht, Nt, d), dtype=torch.uint8, device=dev)
+        n_tr = max(3, min(args.steps // 5, 20))
+        t_f = timed(lambda: fa.forward(qt, kt, vt, out=ot, lse=lt), n_tr, 1) / n_tr
+        t_b = timed(lambda: fa.backward(qt, kt, vt, ot, lt, dot, dq=dq, dk=dk, dv=dv, workspace=ws_b),
+                    n_tr, 1) / n_tr
+        ff = fwd_flops(Bt, Ht, Nt, d)
+        extra["train"] = {"workload": "B=2 H=16 N=8192 d=128 bf16", "fwd_tflops": ff / t_f / 1e12,
+                          "bwd_tflops": 2.5 * ff / t_b / 1e12, "fwd_ms": t_f * 1e3, "bwd_ms": t_b * 1e3,
+                          "fwd_frac_of_bf16_peak": ff / t_f / 1e12 / peak,
+                          "bwd_frac_of_bf16_peak": 2.5 * ff / t_b / 1e12 / peak}
+        fa.device_status()
+
+    if rank != 0:
+        return
+    cpu = None
+    if ws == 1 and not args.no_cpu:
+        cv, rows, secs = oracle_sample(args.cpu_seconds)
+        cpu = {"value": cv, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": f"float64 oracle, {rows} query rows of one prefill head (N=4096, d=128), {secs:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill forward B=4 H=32 N=4096 d=128 bf16, no mask, fp32 accumulation",
+                   "B": B, "H": H, "N": N, "d": d, "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "inputs (3 x 128 MiB) larger than the 129 MB L2, no flush",
+                   "inputs": "torch.randn (seeded Philox) on the device, rounded to bf16"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "kernel": "fwd_bf16_kernel<128>",
+                     "traffic": traffic_for("fwd_prefill", ("fa_fwd.cu", "sm103.cuh"))},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * fa.h — C ABI of libfa.so: exact IO-aware softmax attention on GB300 (sm_103a).
+ *
+ * What is computed.  For every batch b and head h, with scale σ (normally 1/√d):
+ *     S = σ·Q Kᵀ,  P = softmax(S) row-wise,  O = P V,  LSE_i = m_i + ln ℓ_i
+ * where m_i is the row max of S and ℓ_i = Σ_j e^(S_ij − m_i).  This is the
+ * standard attention of "FlashAttention：IO-aware 的注意力 kernel"
+ * (inference-learning-path.pages.dev) §3.1, computed the way its §3.2 describes:
+ * key/value tiles stream through on-chip memory while each query row keeps a
+ * running max m, running normaliser ℓ and an unnormalised accumulator, all
+ * rescaled by e^(m_old − m_new) when the max moves; O/ℓ is taken once at the
+ * end, so the N×N score and probability matrices never reach device memory.
+ *
+ * Conventions shared by every entry point.
+ *   - Tensors are device pointers.  Q, K, V, O, dO, dQ, dK, dV are
+ *     [B, H, N, d] row-major with d innermost, the shape "Q, K, V ∈ R^{N×d}"
+ *     of the FlashAttention walkthrough (kyonqi.github.io, "Flash Attention
+ *     Forward") with batch and head dims in front.  LSE is [B, H, N] float32.
+ *   - LSE uses the natural log of the scaled scores.
+ *   - fa_dtype selects the storage type of Q, K, V, O (and dO, dQ, dK, dV).
+ *     FA_BF16 tensors accumulate in fp32; FA_FP32 computes in fp32 throughout.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on that stream; a call returns after its
+ *     kernels are enqueued.
+ *   - The caller owns and allocates every buffer, including workspaces whose
+ *     size is queried first.  The library allocates no device memory.
+ *   - Errors.  FA_ERR_INVALID_ARG: null pointer, non-positive size, bad
+ *     stride, misaligned pointer (16-byte alignment is required), scale not
+ *     finite and > 0, workspace too small.  FA_ERR_UNSUPPORTED: a head dim,
+ *     dtype or size this build has no kernel for; there is never a silent
+ *     fallback to another algorithm.  FA_ERR_CUDA: a launch or earlier
+ *     asynchronous CUDA error.  FA_ERR_DEVICE_TIMEOUT: a kernel gave up on a
+ *     pipeline wait (reported by fa_device_status).  On any error the
+ *     message is available from fa_get_last_error() in the calling thread.
+ *     Validation happens before anything is enqueued, so an argument error
+ *     leaves the stream untouched.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_DEVICE_TIMEOUT = 4
+} fa_status;
+
+typedef enum fa_dtype { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+/* Version of this ABI; bumped on any incompatible change. */
+FA_API int fa_abi_version(void);
+
+/*
+ * fa_forward — tiled forward pass, one write of O and LSE.
+ *   Follows the lesson's §2 mental model and §3.2 recurrence; the statistics it
+ *   saves are the ones the walkthrough's "Flash Attention Backward" section
+ *   keeps for the backward (here folded into LSE = m + ln ℓ).
+ *   q [B,H,N_q,d], k and v [B,H,N_kv,d]; o [B,H,N_q,d] (same dtype as q);
+ *   lse [B,H,N_q] float32 (may be NULL to skip it).
+ *   strides: NULL for contiguous tensors, or 12 element strides
+ *   {q_b, q_h, q_n, k_b, k_h, k_n, v_b, v_h, v_n, o_b, o_h, o_n}; the d stride is
+ *   always 1 and every stride × element size must be a multiple of 16 bytes.
+ *   N_q may differ from N_kv (query rows are independent).  No mask.
+ *   Supported: FA_BF16 with d ∈ {64, 128} (tensor-core kernel) and FA_FP32 with
+ *   d ∈ {64, 128} (fp32 CUDA-core kernel, for exact checks).
+ */
+FA_API fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int N_q, int N_kv, int d, fa_dtype dtype, float scale,
+                     const int64_t* strides, void* stream);
+
+/*
+ * fa_decode_workspace_size — bytes of workspace fa_decode_splitkv needs:
+ *   the partial outputs B·H·n_splits·d·4 bytes and the partial (m, ℓ) pairs
+ *   B·H·n_splits·2·4 bytes, each rounded up to a multiple of 256.
+ */
+FA_API size_t fa_decode_workspace_size(int B, int H, int d, int n_splits);
+
+/*
+ * fa_decode_splitkv — one query row per head (S_q = 1) against N_kv keys.
+ *   The key range is cut into n_splits contiguous chunks of ceil(N_kv/n_splits)
+ *   keys, processed in parallel ("FlashDecoding", lesson §3.3 and §9: split
+ *   along the KV length to fill the SMs).  Each chunk c yields an unnormalised
+ *   triple (m_c, ℓ_c, o_c); a second kernel folds the triples with the
+ *   block-merge rule of the FlashAttention interview notes (omica.com.cn
+ *   news 1422242, §二.3):  m = max(m_a, m_b), ℓ = ℓ_a e^(m_a−m) + ℓ_b e^(m_b−m),
+ *   o = o_a e^(m_a−m) + o_b e^(m_b−m), and writes O = o/ℓ and LSE = m + ln ℓ.
+ *   q [B,H,1,d], k and v [B,H,N_kv,d] contiguous; o [B,H,1,d]; lse [B,H] (or NULL).
+ *   workspace: device buffer of at least fa_decode_workspace_size() bytes, used
+ *   for the partial triples; its contents on entry do not matter.
+ *   Supported: FA_BF16, d = 128, 1 ≤ n_splits ≤ 256.
+ */
+FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int N_kv, int d, fa_dtype dtype, float scale,
+                            int n_splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_backward_workspace_size — bytes of workspace fa_backward needs:
+ *   fp32 dQ accumulator B·H·N·d·4 plus per-row D and scaled LSE, 2·B·H·N·4,
+ *   each part rounded up to 256.
+ */
+FA_API size_t fa_backward_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_backward — gradients by recomputation.
+ *   The forward kept only O and LSE; S and P are recomputed tile by tile from
+ *   Q, K and LSE ("Flash Attention Backward" in the walkthrough; §二.5 of the
+ *   interview notes).  The gradient itself is not on the pages; this is the
+ *   textbook one for O = softmax(σQKᵀ)V:
+ *     D_i = Σ_t dO_it O_it,  P = e^(S − LSE),  dV = Pᵀ dO,  dP = dO Vᵀ,
+ *     dS = P ∘ (dP − D),  dQ = σ dS K,  dK = σ dSᵀ Q.
+ *   q, k, v, o, dout, dq, dk, dv: [B,H,N,d] contiguous; lse [B,H,N] float32 as
+ *   written by fa_forward.  workspace: at least fa_backward_workspace_size()
+ *   bytes; the library clears what it needs cleared.
+ *   Supported: FA_BF16, d = 128, N a multiple of 128.
+ */
+FA_API fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                      fa_dtype dtype, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * fa_device_status — synchronises `stream`, then reports FA_ERR_DEVICE_TIMEOUT
+ * if any kernel of this library has given up on a bounded pipeline wait since
+ * the last call (and clears that flag), FA_ERR_CUDA on a CUDA error, else FA_OK.
+ */
+FA_API fa_status fa_device_status(void* stream);
+
+/* Static description of a status code. */
+FA_API const char* fa_status_string(fa_status s);
+
+/* Message of the last error raised in the calling thread ("" if none). */
+FA_API const char* fa_get_last_error(void);
+
+/* Number of kernel launches this library has enqueued since it was loaded. */
+FA_API uint64_t fa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

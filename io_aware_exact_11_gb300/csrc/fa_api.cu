@@ -1,0 +1,328 @@
+// fa_api.cu — the C ABI declared in include/fa.h: argument checks, TMA
+// descriptor construction and kernel dispatch.  No device memory is allocated
+// here; every buffer, including workspaces, belongs to the caller.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+std::atomic<uint64_t> g_launches{0};
+
+// One watchdog word per device: kernels write the site of a wait that gave up.
+__device__ unsigned int g_watchdog_word;
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fa_status ok() {
+  g_last_error[0] = '\0';
+  return FA_OK;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Device address of this device's watchdog word (looked up once per device).
+fa_status watchdog_ptr(unsigned int** out) {
+  static std::mutex mu;
+  static unsigned int* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_watchdog_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(watchdog)");
+    cache[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = cache[dev];
+  return FA_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+fa_status get_encoder(EncodeTiledFn* fn) {
+  static std::once_flag once;
+  static EncodeTiledFn cached = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (cached == nullptr) {
+    return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)",
+                err == cudaSuccess ? "symbol not found" : cudaGetErrorString(err));
+  }
+  *fn = cached;
+  return FA_OK;
+}
+
+// 4-D bf16 map over a [B, H, N, d] tensor with element strides (sb, sh, sn),
+// d contiguous; box = 64 head-dim values × 128 rows, 128-byte swizzle; rows
+// past N read as zero.
+fa_status make_map(CUtensorMap* tm, const void* base, int B, int H, int N, int d, int64_t sb, int64_t sh,
+                   int64_t sn, const char* name) {
+  EncodeTiledFn enc;
+  fa_status s = get_encoder(&enc);
+  if (s != FA_OK) return s;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn) * 2, static_cast<cuuint64_t>(sh) * 2,
+                           static_cast<cuuint64_t>(sb) * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return FA_OK;
+}
+
+bool bad_scale(float scale) { return !(std::isfinite(scale) && scale > 0.f); }
+
+fa_status check_launch(const char* what, int n) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed);
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_abi_version(void) { return 1; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* fa_get_last_error(void) { return g_last_error; }
+
+uint64_t fa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                     int N_kv, int d, fa_dtype dtype, float scale, const int64_t* strides, void* stream) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_forward: null tensor pointer");
+  if (B <= 0 || H <= 0 || N_q <= 0 || N_kv <= 0 || d <= 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward: sizes must be positive (B=%d H=%d N_q=%d N_kv=%d d=%d)", B, H,
+                N_q, N_kv, d);
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_forward: unknown dtype %d", dtype);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_forward: head dim %d not built (64, 128)", d);
+  if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_forward: scale must be finite and > 0");
+  if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_forward: B and H must be <= 65535");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward: q, k, v, o must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward: lse must be 4-byte aligned");
+  const int esz = dtype == FA_BF16 ? 2 : 4;
+  int64_t st[12];
+  if (strides == nullptr) {
+    const int64_t nq = static_cast<int64_t>(N_q) * d, nk = static_cast<int64_t>(N_kv) * d;
+    const int64_t def[12] = {H * nq, nq, d, H * nk, nk, d, H * nk, nk, d, H * nq, nq, d};
+    memcpy(st, def, sizeof(st));
+  } else {
+    memcpy(st, strides, sizeof(st));
+    for (int i = 0; i < 12; ++i) {
+      if (st[i] < 0 || (st[i] * esz) % 16 != 0)
+        return fail(FA_ERR_INVALID_ARG, "fa_forward: stride[%d]=%lld must be >= 0 and a multiple of 16 bytes", i,
+                    static_cast<long long>(st[i]));
+    }
+    if (st[2] < d || st[5] < d || st[8] < d || st[11] < d)
+      return fail(FA_ERR_INVALID_ARG, "fa_forward: row strides must be >= d");
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_BF16) {
+    fa::FwdParams p;
+    memset(&p, 0, sizeof(p));
+    fa_status r;
+    if ((r = make_map(&p.tm_q, q, B, H, N_q, d, st[0], st[1], st[2], "q")) != FA_OK) return r;
+    if ((r = make_map(&p.tm_k, k, B, H, N_kv, d, st[3], st[4], st[5], "k")) != FA_OK) return r;
+    if ((r = make_map(&p.tm_v, v, B, H, N_kv, d, st[6], st[7], st[8], "v")) != FA_OK) return r;
+    if ((r = watchdog_ptr(&p.err)) != FA_OK) return r;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Nq = N_q;
+    p.Nkv = N_kv;
+    p.o_sb = st[9];
+    p.o_sh = st[10];
+    p.o_sn = st[11];
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = fa::launch_fwd_bf16(d, p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_forward launch");
+    return check_launch("fa_forward", 1);
+  }
+  fa::FwdF32Params p;
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.o = static_cast<float*>(o);
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Nq = N_q;
+  p.Nkv = N_kv;
+  p.q_sb = st[0]; p.q_sh = st[1]; p.q_sn = st[2];
+  p.k_sb = st[3]; p.k_sh = st[4]; p.k_sn = st[5];
+  p.v_sb = st[6]; p.v_sh = st[7]; p.v_sn = st[8];
+  p.o_sb = st[9]; p.o_sh = st[10]; p.o_sn = st[11];
+  p.scale = scale;
+  cudaError_t e = fa::launch_fwd_f32(d, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_forward (fp32) launch");
+  return check_launch("fa_forward", 1);
+}
+
+size_t fa_decode_workspace_size(int B, int H, int d, int n_splits) {
+  if (B <= 0 || H <= 0 || d <= 0 || n_splits <= 0) return 0;
+  const size_t slots = static_cast<size_t>(B) * H * n_splits;
+  return round256(slots * d * 4) + round256(slots * 2 * 4);
+}
+
+fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int N_kv, int d, fa_dtype dtype, float scale, int n_splits, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !workspace) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: null pointer");
+  if (B <= 0 || H <= 0 || N_kv <= 0 || d <= 0 || n_splits <= 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: sizes must be positive");
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: unknown dtype");
+  if (dtype != FA_BF16 || d != 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv: only bf16 with d=128 is built");
+  if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv: n_splits must be <= 256");
+  if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv: B and H must be <= 65535");
+  if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: scale must be finite and > 0");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: pointers must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: lse must be 4-byte aligned");
+  const size_t need = fa_decode_workspace_size(B, H, d, n_splits);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: workspace %zu bytes, need %zu", workspace_bytes, need);
+  fa::DecodeParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  const size_t slots = static_cast<size_t>(B) * H * n_splits;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(slots * d * 4));
+  p.B = B;
+  p.H = H;
+  p.Nkv = N_kv;
+  p.n_splits = n_splits;
+  p.chunk = (N_kv + n_splits - 1) / n_splits;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  fa_status r = watchdog_ptr(&p.err);
+  if (r != FA_OK) return r;
+  cudaError_t e = fa::launch_decode_bf16(d, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv launch");
+  return check_launch("fa_decode_splitkv", 2);
+}
+
+size_t fa_backward_workspace_size(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round256(rows * d * 4) + 2 * round256(rows * 4);
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_dtype dtype,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return fail(FA_ERR_INVALID_ARG, "fa_backward: null pointer");
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return fail(FA_ERR_INVALID_ARG, "fa_backward: sizes must be positive");
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_backward: unknown dtype");
+  if (dtype != FA_BF16 || d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_backward: only bf16 with d=128 is built");
+  if (N % 128 != 0) return fail(FA_ERR_UNSUPPORTED, "fa_backward: N must be a multiple of 128 (got %d)", N);
+  if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_backward: B and H must be <= 65535");
+  if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_backward: scale must be finite and > 0");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_backward: pointers must be 16-byte aligned (lse 4-byte)");
+  const size_t need = fa_backward_workspace_size(B, H, N, d);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "fa_backward: workspace %zu bytes, need %zu", workspace_bytes, need);
+  fa::BwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int64_t nd = static_cast<int64_t>(N) * d;
+  fa_status r;
+  if ((r = make_map(&p.tm_q, q, B, H, N, d, H * nd, nd, d, "q")) != FA_OK) return r;
+  if ((r = make_map(&p.tm_k, k, B, H, N, d, H * nd, nd, d, "k")) != FA_OK) return r;
+  if ((r = make_map(&p.tm_v, v, B, H, N, d, H * nd, nd, d, "v")) != FA_OK) return r;
+  if ((r = make_map(&p.tm_do, dout, B, H, N, d, H * nd, nd, d, "dout")) != FA_OK) return r;
+  if ((r = watchdog_ptr(&p.err)) != FA_OK) return r;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  char* ws = static_cast<char*>(workspace);
+  p.q = q;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dq_acc = reinterpret_cast<float*>(ws);
+  p.delta = reinterpret_cast<float*>(ws + round256(rows * d * 4));
+  p.lse_log2 = reinterpret_cast<float*>(ws + round256(rows * d * 4) + round256(rows * 4));
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  int launches = 0;
+  cudaError_t e = fa::launch_bwd_bf16(d, p, static_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_backward launch");
+  return check_launch("fa_backward", launches);
+}
+
+fa_status fa_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_device_status: stream sync");
+  unsigned int* word = nullptr;
+  fa_status r = watchdog_ptr(&word);
+  if (r != FA_OK) return r;
+  unsigned int code = 0;
+  e = cudaMemcpy(&code, word, sizeof(code), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_device_status: read watchdog");
+  if (code != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return fail(FA_ERR_DEVICE_TIMEOUT, "kernel %u gave up waiting at site %u", code >> 8, code & 0xFFu);
+  }
+  return ok();
+}
+
+}  // extern "C"

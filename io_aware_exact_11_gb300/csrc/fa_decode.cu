@@ -1,0 +1,224 @@
+// fa_decode.cu — split-KV decode (one query row per head), bf16 in, fp32 math.
+//
+// Decode reads the whole key/value cache once per step and is bound by device
+// memory bandwidth, not by arithmetic ("FlashAttention：IO-aware 的注意力 kernel"
+// §3.3 and §9: the single query's scores are a 1×N vector; FlashDecoding
+// splits the key range across SMs to keep them all busy).
+//
+// Kernel 1 (grid = splits × H × B, 128 threads): CTA c streams keys
+// [c·chunk, (c+1)·chunk) of one (b, h) in sub-chunks of 64 keys.  K and V rows
+// of a sub-chunk are contiguous in memory, so each arrives with one untiled bulk
+// copy per tensor into a 2-stage shared-memory ring.  The CTA runs the online
+// softmax over its keys and writes the unnormalised triple (m_c, ℓ_c, o_c).
+// Kernel 2 (grid = B·H, d threads) folds the triples with the block-merge rule
+// of the FlashAttention interview notes (omica.com.cn news 1422242, §二.3)
+// and writes O = o/ℓ and LSE = m + ln ℓ.
+#include "fa_kernels.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kSub = 64;                      // keys per sub-chunk
+constexpr int kRowBytes = kD * 2;             // one bf16 key row
+constexpr int kStageBytes = 2 * kSub * kRowBytes;  // K then V: 32 KB
+constexpr int kThreads = 128;
+constexpr int kSmem = 2 * kStageBytes + 1024;
+
+struct DecodeSmem {
+  float scores[kSub];
+  float probs[kSub];
+  float red[8][kD];
+  uint64_t full[2];
+  int abort_flag;
+};
+
+__device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernDecode << 8) | s; }
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
+  uint8_t* ring = smem_raw + pad;
+  __shared__ DecodeSmem sm;
+
+  const int c = blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int dchunk = lane & 15;   // 8 head-dim values per lane
+  const int kpar = lane >> 4;     // which of the two keys a warp handles at once
+  const int64_t bh = static_cast<int64_t>(b) * p.H + h;
+  const int key0 = c * p.chunk;
+  const int nkeys = max(0, min(p.Nkv, key0 + p.chunk) - key0);
+  const int nsub = (nkeys + kSub - 1) / kSub;
+
+  const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k) + (bh * p.Nkv + key0) * kRowBytes;
+  const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v) + (bh * p.Nkv + key0) * kRowBytes;
+
+  if (tid == 0) {
+    mbar_init(&sm.full[0], 1);
+    mbar_init(&sm.full[1], 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int i) {
+    const int st = i & 1;
+    const int n = min(kSub, nkeys - i * kSub);
+    const uint32_t bytes = static_cast<uint32_t>(n) * kRowBytes;
+    mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
+    bulk_load(ring + st * kStageBytes, kbase + static_cast<int64_t>(i) * kSub * kRowBytes, bytes, &sm.full[st]);
+    bulk_load(ring + st * kStageBytes + kSub * kRowBytes, vbase + static_cast<int64_t>(i) * kSub * kRowBytes,
+              bytes, &sm.full[st]);
+  };
+  if (tid == 0) {
+    if (nsub > 0) issue(0);
+    if (nsub > 1) issue(1);
+  }
+
+  // This lane's slice of q (8 values), widened to fp32.
+  float qf[8];
+  {
+    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.q) + bh * kRowBytes +
+                                                    dchunk * 16);
+    bf16x8_to_f32(u, qf);
+  }
+  const float sl2 = p.scale_log2;
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+
+  int issued = min(nsub, 2);
+  bool ok = true;
+  for (int i = 0; i < nsub; ++i) {
+    const int st = i & 1;
+    const int n = min(kSub, nkeys - i * kSub);
+    ok = mbar_wait(&sm.full[st], (i >> 1) & 1, &sm.abort_flag, p.err, site(1));
+    if (!__syncthreads_and(ok)) { ok = false; break; }
+    const uint8_t* sK = ring + st * kStageBytes;
+    const uint8_t* sV = sK + kSub * kRowBytes;
+
+    // Scores: each warp takes 16 keys, two at a time (one per half-warp).
+#pragma unroll
+    for (int pr = 0; pr < 8; ++pr) {
+      const int key = warp * 16 + pr * 2 + kpar;
+      float kf[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + key * kRowBytes + dchunk * 16), kf);
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dot = fmaf(qf[e], kf[e], dot);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (dchunk == 0) sm.scores[key] = (key < n) ? dot * sl2 : -INFINITY;
+    }
+    __syncthreads();
+
+    // Online softmax over this sub-chunk (every warp computes the same values).
+    const float s0 = sm.scores[lane];
+    const float s1 = sm.scores[lane + 32];
+    float mx = fmaxf(s0, s1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float m_new = fmaxf(m_run, mx);
+    const float corr = ex2_approx(m_run - m_new);
+    const float p0 = ex2_approx(s0 - m_new);
+    const float p1 = ex2_approx(s1 - m_new);
+    float ps = p0 + p1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    l_run = l_run * corr + ps;
+    m_run = m_new;
+    if (warp == 0) {
+      sm.probs[lane] = p0;
+      sm.probs[lane + 32] = p1;
+    }
+    __syncthreads();
+
+    // P·V: lane owns 8 head-dim values; the 8 (warp, half) groups split the keys.
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= corr;
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) {
+      const int key = ii * 8 + warp * 2 + kpar;
+      if (key < n) {
+        const float pk = sm.probs[key];
+        float vf[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + key * kRowBytes + dchunk * 16), vf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pk, vf[e], acc[e]);
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && i + 2 < nsub) {
+      issue(i + 2);
+      ++issued;
+    }
+  }
+  if (!ok) {
+    if (tid == 0) {
+      for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait_drain(&sm.full[t & 1], (t >> 1) & 1, 200000000ull);
+    }
+    return;
+  }
+
+  // Combine the 8 key groups, then write the unnormalised triple.
+  const int g = warp * 2 + kpar;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sm.red[g][dchunk * 8 + e] = acc[e];
+  __syncthreads();
+  float o = 0.f;
+#pragma unroll
+  for (int gg = 0; gg < 8; ++gg) o += sm.red[gg][tid];
+  const int64_t slot = bh * p.n_splits + c;
+  p.part_o[slot * kD + tid] = o;
+  if (tid == 0) {
+    p.part_ml[slot * 2 + 0] = m_run;  // −∞ and ℓ = 0 for a split with no keys
+    p.part_ml[slot * 2 + 1] = l_run;
+  }
+}
+
+__global__ void __launch_bounds__(kD) decode_merge_kernel(const DecodeParams p) {
+  const int64_t bh = blockIdx.x;
+  const int t = threadIdx.x;
+  const float* ml = p.part_ml + bh * p.n_splits * 2;
+  const float* po = p.part_o + bh * p.n_splits * kD;
+  float m = -INFINITY;
+  for (int c = 0; c < p.n_splits; ++c) m = fmaxf(m, ml[2 * c]);
+  float l = 0.f, o = 0.f;
+  for (int c = 0; c < p.n_splits; ++c) {
+    const float mc = ml[2 * c];
+    const float w = (mc == -INFINITY) ? 0.f : ex2_approx(mc - m);
+    l = fmaf(ml[2 * c + 1], w, l);
+    o = fmaf(po[static_cast<int64_t>(c) * kD + t], w, o);
+  }
+  reinterpret_cast<__nv_bfloat16*>(p.o)[bh * kD + t] = __float2bfloat16_rn(o / l);
+  if (t == 0 && p.lse != nullptr) p.lse[bh] = (m + __log2f(l)) * 0.69314718055994531f;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t stream) {
+  if (d != kD) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,80 @@
+// fa_kernels.h — launch interface between the C ABI (fa_api.cu) and the
+// kernel translation units.  Internal to libfa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Watchdog codes written to the device error word: (kernel << 8) | wait site.
+enum : unsigned int {
+  kKernFwd = 1,
+  kKernDecode = 2,
+  kKernBwd = 3,
+};
+
+struct FwdParams {
+  CUtensorMap tm_q;  // 4-D maps {d, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;
+  float* lse;  // may be null
+  int B, H, Nq, Nkv;
+  int64_t o_sb, o_sh, o_sn;  // element strides of O
+  float scale_log2;          // σ·log2(e)
+  unsigned int* err;
+};
+
+struct FwdF32Params {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* o;
+  float* lse;
+  int B, H, Nq, Nkv;
+  int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn, o_sb, o_sh, o_sn;
+  float scale;
+};
+
+struct DecodeParams {
+  const void* q;  // [B,H,d] bf16
+  const void* k;  // [B,H,N,d] bf16
+  const void* v;
+  void* o;        // [B,H,d] bf16
+  float* lse;     // [B,H] or null
+  float* part_o;  // [B,H,S,d] fp32
+  float* part_ml; // [B,H,S,2] fp32: (m in log2 units, ℓ)
+  int B, H, Nkv, n_splits, chunk;
+  float scale_log2;
+  unsigned int* err;
+};
+
+struct BwdParams {
+  CUtensorMap tm_q;   // {d, N, H, B}, box {64, 128, 1, 1}
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const void* q;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;      // [B,H,N,d] fp32, zeroed before the main kernel
+  float* delta;       // [B,H,N]   D_i
+  float* lse_log2;    // [B,H,N]   LSE·log2(e)
+  int B, H, N;
+  float scale;        // σ
+  float scale_log2;   // σ·log2(e)
+  unsigned int* err;
+};
+
+cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_f32(int d, const FwdF32Params& p, cudaStream_t s);
+cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t s, int* launches);
+
+}  // namespace fa

@@ -1,0 +1,208 @@
+"""ctypes binding for libfa.so (the C ABI in include/fa.h).
+
+Argument marshalling only: tensors are passed as raw device pointers plus
+sizes and strides, on the caller's current CUDA stream.  PyTorch provides
+device memory and streams; every step of the computation runs in the
+library's CUDA kernels.  If libfa.so has not been built this module raises,
+there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfa.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(5)
+FA_BF16, FA_FP32 = 0, 1
+
+EXPORTED = (
+    "fa_abi_version",
+    "fa_forward",
+    "fa_decode_workspace_size",
+    "fa_decode_splitkv",
+    "fa_backward_workspace_size",
+    "fa_backward",
+    "fa_device_status",
+    "fa_status_string",
+    "fa_get_last_error",
+    "fa_launch_count",
+)
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[status {status}] {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Open libfa.so once (raises FileNotFoundError if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FileNotFoundError(
+                f"{LIB_PATH} is missing: build it with `python -m io_aware_exact_11_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.fa_abi_version.restype = i32
+        L.fa_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp]
+        L.fa_forward.restype = i32
+        L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.fa_decode_workspace_size.restype = sz
+        L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+        L.fa_decode_splitkv.restype = i32
+        L.fa_backward_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.fa_backward_workspace_size.restype = sz
+        L.fa_backward.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, vp, sz, vp]
+        L.fa_backward.restype = i32
+        L.fa_device_status.argtypes = [vp]
+        L.fa_device_status.restype = i32
+        L.fa_status_string.argtypes = [i32]
+        L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_get_last_error.restype = ctypes.c_char_p
+        L.fa_launch_count.restype = ctypes.c_uint64
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != FA_OK:
+        msg = lib().fa_get_last_error().decode(errors="replace")
+        raise FAError(status, msg or lib().fa_status_string(status).decode())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must live on a CUDA device")
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued since it was loaded."""
+    return int(lib().fa_launch_count())
+
+
+def device_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel's bounded wait gave up."""
+    _check(lib().fa_device_status(_stream_ptr(stream)))
+
+
+def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True, stream=None):
+    """Exact attention forward.  q [B,H,Nq,d], k/v [B,H,Nkv,d] (bf16 or fp32).
+
+    Returns (O, LSE) with O like q and LSE fp32 [B,H,Nq].  Non-contiguous
+    inputs are passed by stride (d must be the contiguous dim).
+    """
+    torch = _torch()
+    _check_cuda(q, k, v)
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    if k.shape != (B, H, Nkv, d) or v.shape != (B, H, Nkv, d):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    strides = None
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous() and out.is_contiguous()):
+        for t in (q, k, v, out):
+            if t.stride(3) != 1:
+                raise ValueError("the head dim must be contiguous")
+        arr = (ctypes.c_int64 * 12)(*[int(t.stride(i)) for t in (q, k, v, out) for i in range(3)])
+        strides = ctypes.cast(arr, ctypes.c_void_p)
+    _check(lib().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d,
+                            _dtype_code(q), float(scale), strides, _stream_ptr(stream)))
+    return out, lse
+
+
+def decode_workspace_size(B: int, H: int, d: int, n_splits: int) -> int:
+    return int(lib().fa_decode_workspace_size(B, H, d, n_splits))
+
+
+def decode_splitkv(q, k, v, n_splits: int = 32, scale: float | None = None, out=None, lse=None,
+                   workspace=None, stream=None):
+    """Split-KV decode: q [B,H,1,d] against k/v [B,H,Nkv,d]; returns (O, LSE)."""
+    torch = _torch()
+    _check_cuda(q, k, v)
+    B, H, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query row per head")
+    Nkv = k.shape[2]
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("decode inputs must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, 1, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(B, H, d, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nkv, d,
+                                   _dtype_code(q), float(scale), int(n_splits), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+def backward_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().fa_backward_workspace_size(B, H, N, d))
+
+
+def backward(q, k, v, o, lse, do, scale: float | None = None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients (dQ, dK, dV) from the saved O and LSE; all [B,H,N,d] contiguous."""
+    torch = _torch()
+    _check_cuda(q, k, v, o, lse, do)
+    B, H, N, d = q.shape
+    for t in (q, k, v, o, do):
+        if tuple(t.shape) != (B, H, N, d) or not t.is_contiguous():
+            raise ValueError("backward tensors must be contiguous [B,H,N,d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = backward_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                             _ptr(dv), B, H, N, d, _dtype_code(q), float(scale), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return dq, dk, dv

@@ -1,0 +1,50 @@
+"""Shared helpers for the GPU parity tests: seeded inputs on the device and
+error metrics.  Inputs come from the seeded generator only; expected values
+come from the float64 oracle only."""
+
+from __future__ import annotations
+
+import numpy as np
+
+from io_aware_exact_11_gb300 import inputs
+
+
+def to_device(host: np.ndarray, dtype: str):
+    """Host tensor from ``inputs.normal_tensor`` -> CUDA tensor (bf16 or fp32)."""
+    import torch
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(host).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(host))
+    return t.cuda()
+
+
+def make_qkv(seed: int, B: int, H: int, Nq: int, Nkv: int, d: int, dtype: str, with_do: bool = False):
+    """Host arrays (storage type) and device tensors for Q, K, V (and dO)."""
+    host = {
+        "q": inputs.normal_tensor(seed, "q", B, H, Nq, d, dtype),
+        "k": inputs.normal_tensor(seed, "k", B, H, Nkv, d, dtype),
+        "v": inputs.normal_tensor(seed, "v", B, H, Nkv, d, dtype),
+    }
+    if with_do:
+        host["do"] = inputs.normal_tensor(seed, "do", B, H, Nq, d, dtype)
+    dev = {k: to_device(v, dtype) for k, v in host.items()}
+    return host, dev
+
+
+def f64(host: np.ndarray, dtype: str) -> np.ndarray:
+    return inputs.as_f64(host, dtype)
+
+
+def max_abs(a, b) -> float:
+    return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))))
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def cpu64(t) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)

@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/fa.h declares, and rejects bad arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from io_aware_exact_11_gb300 import fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(fa.LIB_PATH):
+        from io_aware_exact_11_gb300 import build
+        build.build()
+    return fa.lib()
+
+
+def test_header_declares_expected_entry_points():
+    assert set(_declared()) == set(fa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert L.fa_abi_version() == 1
+    for s in range(5):
+        assert L.fa_status_string(s)
+    assert L.fa_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(L):
+    assert L.fa_decode_workspace_size(64, 32, 128, 32) == 64 * 32 * 32 * 128 * 4 + 64 * 32 * 32 * 2 * 4
+    assert L.fa_decode_workspace_size(1, 1, 128, 3) == 1536 + 256
+    assert L.fa_decode_workspace_size(0, 1, 128, 3) == 0
+    rows = 2 * 16 * 8192
+    assert L.fa_backward_workspace_size(2, 16, 8192, 128) == rows * 128 * 4 + 2 * rows * 4
+    assert L.fa_backward_workspace_size(1, 1, 5, 128) == 2560 + 2 * 256
+
+
+FAKE = ctypes.c_void_p(1 << 20)        # never dereferenced: validation fails first
+FAKE_BAD = ctypes.c_void_p((1 << 20) + 4)
+
+
+def _fwd(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=1, Nq=128, Nkv=128, d=128, dt=fa.FA_BF16,
+             scale=0.1, strides=None, stream=None)
+    a.update(kw)
+    return L.fa_forward(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nkv"], a["d"],
+                        a["dt"], a["scale"], a["strides"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nkv=-3), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(dt=7), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(k=FAKE_BAD), fa.FA_ERR_INVALID_ARG),
+    (dict(H=70000), fa.FA_ERR_UNSUPPORTED),
+])
+def test_forward_rejects_bad_arguments(L, kw, status):
+    assert _fwd(L, **kw) == status
+    assert L.fa_get_last_error()
+
+
+def test_forward_rejects_bad_strides(L):
+    st = (ctypes.c_int64 * 12)(*([128 * 128, 128 * 128, 128] * 3 + [128 * 128, 128 * 128, 100]))
+    assert _fwd(L, strides=ctypes.cast(st, ctypes.c_void_p)) == fa.FA_ERR_INVALID_ARG
+    assert b"stride" in L.fa_get_last_error()
+    st2 = (ctypes.c_int64 * 12)(*([128 * 128, 128 * 128, 64] * 4))
+    assert _fwd(L, strides=ctypes.cast(st2, ctypes.c_void_p)) == fa.FA_ERR_INVALID_ARG
+
+
+def test_decode_rejects_bad_arguments(L):
+    def dec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=2, H=2, N=256, d=128, dt=fa.FA_BF16, scale=0.1,
+                 ns=4, ws=FAKE, wsb=1 << 20, stream=None)
+        a.update(kw)
+        return L.fa_decode_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                                   a["dt"], a["scale"], a["ns"], a["ws"], a["wsb"], a["stream"])
+    assert dec(ws=None) == fa.FA_ERR_INVALID_ARG
+    assert dec(wsb=100) == fa.FA_ERR_INVALID_ARG
+    assert b"workspace" in L.fa_get_last_error()
+    assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert dec(dt=fa.FA_FP32) == fa.FA_ERR_UNSUPPORTED
+    assert dec(ns=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(ns=257) == fa.FA_ERR_UNSUPPORTED
+    assert dec(N=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(q=FAKE_BAD) == fa.FA_ERR_INVALID_ARG
+
+
+def test_backward_rejects_bad_arguments(L):
+    def bwd(**kw):
+        a = dict(B=1, H=1, N=256, d=128, dt=fa.FA_BF16, scale=0.1, ws=FAKE, wsb=1 << 24)
+        a.update(kw)
+        return L.fa_backward(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
+                             a["dt"], a["scale"], a["ws"], a["wsb"], None)
+    assert bwd(N=200) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(wsb=10) == fa.FA_ERR_INVALID_ARG
+    assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert bwd(ws=None) == fa.FA_ERR_INVALID_ARG
