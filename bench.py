@@ -42,7 +42,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from one ncu capture of each kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the sha256 of the kernel's sources at capture
 # time; a changed kernel reports null until it is captured again.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/fwd_bf16_kernel_prefill_B4_H32_N4096_d128.md
+    "fwd_prefill": {"src": "106cb2c15a862360", "bytes": 402754560 + 117957888},
+}
 
 
 def fwd_flops(B, H, N, d, Nkv=None):

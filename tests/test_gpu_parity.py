@@ -69,16 +69,23 @@ def test_forward_bf16_matches_oracle(shape):
 
 
 def test_forward_bf16_large_scores():
-    """Scores of magnitude ~50 exercise the running-max rescale."""
+    """Scores with standard deviation ~6 exercise the running-max rescale.
+
+    Bound derived from the arithmetic rather than the N(0,1) tolerance: the
+    probabilities enter P·V rounded to bf16 (relative error <= 2^-9, so at most
+    2^-9·max|V| in O) and O is stored as bf16 (<= 2^-9·|O|).  With peaked rows
+    |O| approaches max|V|, so the bound is 2^-8·max|V| plus fp32 noise.  LSE is
+    fp32 throughout: its error scales with its magnitude (~1e-6 relative).
+    """
     import torch
     B, H, N, d = 1, 2, 512, 128
     host, dev = make_qkv(5, B, H, N, N, d, "bf16")
     q = (dev["q"].float() * 6).to(torch.bfloat16)
     o, lse = fa.forward(q, dev["k"], dev["v"])
-    ref_o, ref_lse = oracle.attention_forward(cpu64(q), f64(host["k"], "bf16"), f64(host["v"], "bf16"),
-                                              1 / math.sqrt(d))
-    assert max_abs(cpu64(o), ref_o) <= TOL_O_BF16
-    assert max_abs(cpu64(lse), ref_lse) <= 4 * TOL_LSE_BF16 * max(1.0, float(np.abs(ref_lse).max()) / 10)
+    v64 = f64(host["v"], "bf16")
+    ref_o, ref_lse = oracle.attention_forward(cpu64(q), f64(host["k"], "bf16"), v64, 1 / math.sqrt(d))
+    assert max_abs(cpu64(o), ref_o) <= 2.0 ** -8 * float(np.abs(v64).max()) + 1e-3
+    assert max_abs(cpu64(lse), ref_lse) <= TOL_LSE_BF16 * max(1.0, float(np.abs(ref_lse).max()) / 8)
 
 
 def test_forward_strided_inputs():
@@ -184,8 +191,8 @@ def test_decode_matches_forward_kernel():
     _, dev = make_qkv(8, 2, 4, 1, 2048, 128, "bf16")
     o1, l1 = fa.decode_splitkv(dev["q"], dev["k"], dev["v"], n_splits=32)
     o2, l2 = fa.forward(dev["q"], dev["k"], dev["v"])
-    assert max_abs(cpu64(o1), cpu64(o2)) <= 2 * TOL_O_BF16 / 2
-    assert max_abs(cpu64(l1), cpu64(l2)) <= TOL_LSE_BF16
+    assert max_abs(cpu64(o1), cpu64(o2)) <= TOL_O_BF16
+    assert max_abs(cpu64(l1), cpu64(l2)[..., 0]) <= TOL_LSE_BF16
 
 
 @pytest.mark.slow
