@@ -108,6 +108,34 @@ FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, 
                             int n_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_decode_splitkv_noalloc — fa_decode_splitkv for callers that cannot pass a
+ * workspace.  The pages have no counterpart: this is a deployment variant.
+ *   Who it is for: callers that cannot allocate device memory when they decode,
+ *   e.g. a serving process whose KV cache has reserved nearly all of the GPU's
+ *   memory up front (a cudaMalloc at decode time would fail or force a
+ *   synchronising reallocation), or a host program that reaches the library
+ *   only through this C function and has no device allocator of its own.
+ *   Arguments and results are those of fa_decode_splitkv without `workspace`
+ *   and `workspace_bytes`.  The partial triples go to a fixed scratch buffer of
+ *   FA_DECODE_STATIC_SCRATCH_BYTES (36 MiB) compiled into libfa.so, which every
+ *   GPU that loads the library holds until the process exits.  If
+ *   fa_decode_workspace_size(B, H, d, n_splits) is larger than that buffer the
+ *   call returns FA_ERR_UNSUPPORTED and enqueues nothing (36 MiB covers, e.g.,
+ *   B·H = 2048 heads with 32 splits at d = 128).
+ *   The first call on a device looks up the buffer's device address with that
+ *   device current; make that first call before any stream capture begins.
+ *   Every call shares the one buffer, which keeps the last call's contents; each
+ *   call rewrites every partial it reads, so nothing needs clearing.  Calls whose
+ *   work overlaps on the GPU (other streams, other host threads) race on the
+ *   buffer: the caller must serialise them.
+ *   This entry point calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define FA_DECODE_STATIC_SCRATCH_BYTES ((size_t)36 << 20)
+FA_API fa_status fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                           int B, int H, int N_kv, int d, fa_dtype dtype, float scale,
+                                           int n_splits, void* stream);
+
+/*
  * fa_backward_workspace_size — bytes of workspace fa_backward needs:
  *   fp32 dQ accumulator B·H·N·d·4 plus per-row D and scaled LSE, 2·B·H·N·4,
  *   each part rounded up to 256.

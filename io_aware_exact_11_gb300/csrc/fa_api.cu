@@ -253,6 +253,55 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
   return check_launch("fa_decode_splitkv", 2);
 }
 
+// Same kernels as fa_decode_splitkv; the partial triples live in the library's
+// own scratch buffer (fa_decode.cu) instead of a caller workspace.
+fa_status fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                    int N_kv, int d, fa_dtype dtype, float scale, int n_splits, void* stream) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: null pointer");
+  if (B <= 0 || H <= 0 || N_kv <= 0 || d <= 0 || n_splits <= 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: sizes must be positive");
+  if (dtype != FA_BF16 && dtype != FA_FP32)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: unknown dtype");
+  if (dtype != FA_BF16 || d != 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_noalloc: only bf16 with d=128 is built");
+  if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_noalloc: n_splits must be <= 256");
+  if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_noalloc: B and H must be <= 65535");
+  if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: scale must be finite and > 0");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: pointers must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: lse must be 4-byte aligned");
+  const size_t need = fa_decode_workspace_size(B, H, d, n_splits);
+  if (need > fa::kDecodeStaticScratchBytes)
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_splitkv_noalloc: needs %zu bytes of scratch, the built-in buffer holds %zu "
+                "(use fa_decode_splitkv with a workspace)",
+                need, fa::kDecodeStaticScratchBytes);
+  void* scratch = nullptr;
+  cudaError_t e = fa::decode_static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_noalloc: scratch address");
+  fa::DecodeParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  const size_t slots = static_cast<size_t>(B) * H * n_splits;
+  p.part_o = static_cast<float*>(scratch);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + round256(slots * d * 4));
+  p.B = B;
+  p.H = H;
+  p.Nkv = N_kv;
+  p.n_splits = n_splits;
+  p.chunk = (N_kv + n_splits - 1) / n_splits;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  fa_status r = watchdog_ptr(&p.err);
+  if (r != FA_OK) return r;
+  e = fa::launch_decode_bf16(d, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_noalloc launch");
+  return check_launch("fa_decode_splitkv_noalloc", 2);
+}
+
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N;

@@ -13,6 +13,8 @@
 // Kernel 2 (grid = B·H, d threads) folds the triples with the block-merge rule
 // of the FlashAttention interview notes (omica.com.cn news 1422242, §二.3)
 // and writes O = o/ℓ and LSE = m + ln ℓ.
+#include <mutex>
+
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -219,6 +221,39 @@ cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t stream
   if (e != cudaSuccess) return e;
   decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace fa
+
+// ----------------------------------------------------- library-owned scratch
+// Scratch for fa_decode_splitkv_noalloc: the partial triples live in this
+// fixed buffer instead of a caller workspace.  Every device that loads the
+// library holds it until the process exits.  In host code the name is only a
+// stand-in; the device address comes from cudaGetSymbolAddress below.
+namespace fa {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeStaticScratchBytes];
+
+}  // namespace
+
+cudaError_t decode_static_scratch(void** out) {
+  static std::mutex mu;
+  static void* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    // Once per device, with that device current.
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return cudaSuccess;
 }
 
 }  // namespace fa

@@ -77,4 +77,9 @@ cudaError_t launch_fwd_f32(int d, const FwdF32Params& p, cudaStream_t s);
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t s, int* launches);
 
+// Size of the library-owned decode scratch (fa_decode_splitkv_noalloc).
+constexpr size_t kDecodeStaticScratchBytes = static_cast<size_t>(36) << 20;
+// Device address of that scratch on the current device (looked up once per device).
+cudaError_t decode_static_scratch(void** out);
+
 }  // namespace fa

@@ -24,6 +24,7 @@ EXPORTED = (
     "fa_forward",
     "fa_decode_workspace_size",
     "fa_decode_splitkv",
+    "fa_decode_splitkv_noalloc",
     "fa_backward_workspace_size",
     "fa_backward",
     "fa_device_status",
@@ -178,6 +179,41 @@ def decode_splitkv(q, k, v, n_splits: int = 32, scale: float | None = None, out=
     _check(lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nkv, d,
                                    _dtype_code(q), float(scale), int(n_splits), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+DECODE_STATIC_SCRATCH_BYTES = 36 << 20
+
+
+def decode_splitkv_noalloc(q, k, v, n_splits: int = 32, scale: float | None = None, out=None, lse=None,
+                           stream=None):
+    """Split-KV decode whose scratch is the library's fixed 36 MiB buffer.
+
+    For callers that cannot provide device workspace (no allocator at decode
+    time).  The library allocates nothing; `out` and `lse` are allocated here
+    only when not given.  Calls overlapping on the GPU race on the buffer.
+    """
+    torch = _torch()
+    _check_cuda(q, k, v)
+    L = lib()
+    fn = L.fa_decode_splitkv_noalloc
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+    fn.restype = i32
+    B, H, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query row per head")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("decode inputs must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, 1, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, k.shape[2], d, _dtype_code(q), float(scale),
+              int(n_splits), _stream_ptr(stream)))
     return out, lse
 
 
