@@ -1,46 +1,61 @@
 // fa_fwd.cu — forward attention on tcgen05 tensor cores (bf16 in, fp32 accumulate).
 //
-// One CTA owns a 128-row tile Q_i of one (b, h) and streams all key/value tiles
-// K_j, V_j (128 keys each) past it, as in the two-loop structure of
-// "FlashAttention：IO-aware 的注意力 kernel" §2 / §3.3 (outer loop over query
-// tiles, inner loop over key/value tiles).  Per key tile:
-//   S_j = Q_i K_jᵀ                       tcgen05.mma into TMEM (fp32)
-//   m_new = max(m, rowmax(σ S_j))        softmax warps, one thread per row
-//   P̃ = e^(σS_j − m_new), ℓ = e^(m−m_new)ℓ + rowsum(P̃)      (§3.2)
-//   O = e^(m−m_new) O + P̃ V_j            rescale in TMEM, then tcgen05.mma
-// and after the last tile O/ℓ and LSE = m + ln ℓ are written once.
+// One CTA owns two 128-row query tiles Q_0, Q_1 (256 consecutive rows) of one
+// (b, h) and streams every key/value tile K_j, V_j (128 keys) past both, as in
+// the two-loop structure of "FlashAttention：IO-aware 的注意力 kernel" §2 / §3.3
+// (outer loop over query tiles, inner loop over key/value tiles).  Per key tile
+// and per query tile i:
+//   S_i = Q_i K_jᵀ                        tcgen05.mma into TMEM (fp32)
+//   m_new = max(m, rowmax(σ S_i))         softmax warps, one thread per row
+//   P̃ = e^(σS_i − m_new), ℓ = e^(m−m_new)ℓ + rowsum(P̃)      (§3.2)
+//   O_i = e^(m−m_new) O_i + P̃ V_j         rescale in TMEM, then tcgen05.mma
+// and after the last tile O_i/ℓ and LSE = m + ln ℓ are written once.
 // Exponentials run in base 2 with σ·log2(e) folded into the scores.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K_j / V_j into a 2-stage ring
-//   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 2..5  softmax / rescale / epilogue; warp w reads TMEM lanes 32·(w%4)+…
-// TMEM: two S buffers (columns 0..255) so S_{j+1} is computed while the
-// softmax of tile j runs, and the O accumulator at column 256.
+// Warp roles (320 threads):
+//   warp 0       TMA producer: Q_0, Q_1 once, then K_0, K_1, V_0, K_2, V_1, …
+//                (keys run one tile ahead) into a 3-slot shared-memory ring
+//   warp 1       TMEM owner and MMA issuer (one thread); per key tile it issues
+//                S_0(j), S_1(j), then P̃_0(j−1)V_{j−1}, P̃_1(j−1)V_{j−1}
+//   warps 2..5   softmax / rescale / epilogue of Q_0 (warp w reads TMEM lanes 32·(w%4)…)
+//   warps 6..9   the same for Q_1
+// Two softmax warpgroups put two independent softmax warps on every SM
+// sub-partition, so one's exponentials and TMEM loads overlap the other's, and
+// the tensor cores always have the other tile's MMAs queued.  Sharing each
+// K/V tile between two query tiles also halves the L2 → SM traffic.
+// TMEM: S_0 (columns 0..127), S_1 (128..255), O_0 (256..), O_1 (384..).
 // Shared memory holds every operand in the 128-byte-swizzled layout TMA writes:
-// blocks of [128 rows][64 bf16].
+// blocks of [128 rows][64 bf16]; P̃_i is written there by its softmax warps.
+//
+// Lazy rescaling: a row keeps its reference max m until a tile's max exceeds
+// it by more than kRescaleLog2 (base-2 units).  Until then P̃ = 2^(σ'S − m) is
+// at most 2^kRescaleLog2 and O, ℓ keep accumulating against the same m, so the
+// final O/ℓ and LSE = m + ln ℓ are the same numbers in exact arithmetic; only
+// when the max really moves is O rescaled in TMEM by e^(m_old − m_new).
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBM = 128;          // rows per query tile
+constexpr int kQT = 2;            // query tiles per CTA
+constexpr int kBN = 128;          // keys per key/value tile
 constexpr int kTileBytes = 128 * 128;  // one [128 rows][64 bf16] swizzled block
-constexpr int kThreads = 192;
+constexpr int kThreads = 64 + kQT * 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kNKB = D / 64;  // 128-byte blocks along the head dim
-  static constexpr int kStages = 2;
+  static constexpr int kNKB = D / 64;               // 128-byte blocks along the head dim
+  static constexpr int kSlot = kNKB * kTileBytes;   // one Q, K or V tile
+  static constexpr int kRing = 3;                   // K_j, V_j, K_{j+1} in flight
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kNKB * kTileBytes;
-  static constexpr int kV = kK + kStages * kNKB * kTileBytes;
-  static constexpr int kP = kV + kStages * kNKB * kTileBytes;
-  static constexpr int kBar = kP + 2 * kTileBytes;
+  static constexpr int kR = kQ + kQT * kSlot;
+  static constexpr int kP = kR + kRing * kSlot;     // one P̃ tile per query tile
+  static constexpr int kBar = kP + kQT * 2 * kTileBytes;
   static constexpr int kUsed = kBar + 512;
   // +1 KB so the base can be rounded up to 1024; at least 120 KB so only one
   // CTA (which owns all 512 TMEM columns) is resident per SM.
@@ -49,14 +64,21 @@ struct FwdLayout {
 
 struct FwdBars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, drain;
+  uint64_t r_full[3], r_empty[3];
+  uint64_t s_full[kQT], s_free[kQT];
+  uint64_t p_full[kQT], p_free[kQT];  // p_free[i]: the P̃_i V MMA has finished
+  uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernFwd << 8) | s; }
+
+// Position in the load sequence K_0, K_1, V_0, K_2, V_1, K_3, …, V_{T−1}: keys run
+// one tile ahead of values, which is also the order the MMA warp consumes them
+// (S(j) needs K_j; P̃(j−1)V_{j−1} is issued right after it).
+__device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int seq_v(int j, int T) { return min(2 * j + 2, 2 * T - 1); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
@@ -69,23 +91,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM;
+  const int m0 = blockIdx.x * (kQT * kBM);
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int T = (p.Nkv + kBN - 1) / kBN;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 128);
+    for (int s = 0; s < L::kRing; ++s) {
+      mbar_init(&bars->r_full[s], 1);
+      mbar_init(&bars->r_empty[s], 1);
     }
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->o_done, 1);
+    for (int i = 0; i < kQT; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], 128);
+      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_free[i], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -105,33 +127,35 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, L::kNKB * kTileBytes);
-      for (int kb = 0; kb < L::kNKB; ++kb)
-        tma_load_4d(smem + L::kQ + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64, m0, h, b);
-      int nk = 0, nv = 0;
-      for (int j = 0; j < T; ++j) {
-        const int s = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort_flag, p.err, site(1))) break;
-        mbar_arrive_expect_tx(&bars->k_full[s], L::kNKB * kTileBytes);
+      mbar_arrive_expect_tx(&bars->q_full, kQT * L::kSlot);
+      for (int i = 0; i < kQT; ++i)
         for (int kb = 0; kb < L::kNKB; ++kb)
-          tma_load_4d(smem + L::kK + (s * L::kNKB + kb) * kTileBytes, &p.tm_k, &bars->k_full[s], kb * 64,
-                      j * kBN, h, b);
-        ++nk;
-        if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort_flag, p.err, site(2))) break;
-        mbar_arrive_expect_tx(&bars->v_full[s], L::kNKB * kTileBytes);
+          tma_load_4d(smem + L::kQ + i * L::kSlot + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64,
+                      m0 + i * kBM, h, b);
+      // Load t (sequence K_0, K_1, V_0, K_2, V_1, …, V_{T−1}) goes to slot t % 3.
+      int issued = 0;
+      for (int t = 0; t < 2 * T; ++t) {
+        const int slot = t % L::kRing;
+        const uint32_t u = t / L::kRing;
+        bool is_v;
+        int jt;
+        if (t == 0) { is_v = false; jt = 0; }
+        else if (t == 2 * T - 1) { is_v = true; jt = T - 1; }
+        else if (t & 1) { is_v = false; jt = (t + 1) >> 1; }
+        else { is_v = true; jt = (t - 2) >> 1; }
+        if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        mbar_arrive_expect_tx(&bars->r_full[slot], L::kSlot);
+        const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
         for (int kb = 0; kb < L::kNKB; ++kb)
-          tma_load_4d(smem + L::kV + (s * L::kNKB + kb) * kTileBytes, &p.tm_v, &bars->v_full[s], kb * 64,
-                      j * kBN, h, b);
-        ++nv;
+          tma_load_4d(smem + L::kR + slot * L::kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
+                      jt * kBN, h, b);
+        ++issued;
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
         mbar_wait_drain(&bars->q_full, 0, 200000000ull);
-        for (int t = (nk > L::kStages ? nk - L::kStages : 0); t < nk; ++t)
-          mbar_wait_drain(&bars->k_full[t % L::kStages], (t / L::kStages) & 1, 200000000ull);
-        for (int t = (nv > L::kStages ? nv - L::kStages : 0); t < nv; ++t)
-          mbar_wait_drain(&bars->v_full[t % L::kStages], (t / L::kStages) & 1, 200000000ull);
+        for (int t = (issued > L::kRing ? issued - L::kRing : 0); t < issued; ++t)
+          mbar_wait_drain(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, 200000000ull);
       }
     }
   } else if (warp == 1) {
@@ -140,45 +164,49 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
       const uint32_t sQ = smem_u32(smem + L::kQ);
-      const uint32_t sK = smem_u32(smem + L::kK);
-      const uint32_t sV = smem_u32(smem + L::kV);
+      const uint32_t sR = smem_u32(smem + L::kR);
       const uint32_t sP = smem_u32(smem + L::kP);
-      auto issue_pv = [&](int i) -> bool {
-        const int s = i % L::kStages;
-        const uint32_t ph = (i / L::kStages) & 1;
-        if (!mbar_wait(&bars->p_full, i & 1, abort_flag, p.err, site(3))) return false;
-        if (!mbar_wait(&bars->v_full[s], ph, abort_flag, p.err, site(4))) return false;
-        tc_fence_after();
-        const uint32_t vb = sV + s * L::kNKB * kTileBytes;
+      auto issue_pv = [&](int jj) -> bool {
+        const int t = seq_v(jj, T);
+        const int slot = t % L::kRing;
+        if (!mbar_wait(&bars->r_full[slot], (t / L::kRing) & 1, abort_flag, p.err, site(3))) return false;
+        const uint32_t vb = sR + slot * L::kSlot;
+        for (int i = 0; i < kQT; ++i) {
+          if (!mbar_wait(&bars->p_full[i], jj & 1, abort_flag, p.err, site(4))) return false;
+          tc_fence_after();
+          const uint32_t pbuf = sP + i * 2 * kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // A = P̃ (K-major, keys along K); B = V_j (MN-major: head dim contiguous).
-          const uint64_t ad = sdesc_sw128(sP + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTileBytes, 1024);
-          mma_bf16_ss(tmem + kColO, ad, bd, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            // A = P̃_i (K-major, keys along K); B = V_j (MN-major: head dim contiguous).
+            const uint64_t ad = sdesc_sw128(pbuf + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTileBytes, 1024);
+            mma_bf16_ss(tmem + kColO + i * 128, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->p_free[i]);
         }
-        mma_commit(&bars->o_done);
-        mma_commit(&bars->v_empty[s]);
+        mma_commit(&bars->r_empty[slot]);
         return true;
       };
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, site(5));
       for (int j = 0; ok && j < T; ++j) {
-        const int s = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        const int sb = j & 1;
-        ok = mbar_wait(&bars->k_full[s], ph, abort_flag, p.err, site(6)) &&
-             mbar_wait(&bars->s_free[sb], ((j >> 1) & 1) ^ 1, abort_flag, p.err, site(7));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = sK + s * L::kNKB * kTileBytes;
+        const int t = seq_k(j);
+        const int slot = t % L::kRing;
+        if (!(ok = mbar_wait(&bars->r_full[slot], (t / L::kRing) & 1, abort_flag, p.err, site(6)))) break;
+        const uint32_t kb = sR + slot * L::kSlot;
+        for (int i = 0; i < kQT && ok; ++i) {
+          if (!(ok = mbar_wait(&bars->s_free[i], (j & 1) ^ 1, abort_flag, p.err, site(7)))) break;
+          tc_fence_after();
+          const uint32_t qb = sQ + i * L::kSlot;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + sb * kBN, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                      kIdescS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+            mma_bf16_ss(tmem + i * kBN, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                        kIdescS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[i]);
         }
-        mma_commit(&bars->s_full[sb]);
-        mma_commit(&bars->k_empty[s]);
+        if (!ok) break;
+        mma_commit(&bars->r_empty[slot]);
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) issue_pv(T - 1);
@@ -189,21 +217,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------- softmax / epilogue
-    const int wq = warp & 3;
+    const int qt = (warp - 2) >> 2;          // which query tile
+    const int wq = warp & 3;                 // TMEM lane quarter
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_col = qt * kBN;
+    const uint32_t o_col = kColO + qt * 128;
     const float sl2 = p.scale_log2;
-    uint8_t* sP = smem + L::kP;
+    uint8_t* pbuf = smem + L::kP + qt * 2 * kTileBytes;
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(&bars->s_full[sb], (j >> 1) & 1, abort_flag, p.err, site(8));
+      ok = mbar_wait(&bars->s_full[qt], j & 1, abort_flag, p.err, site(8));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
-      const uint32_t sa = tmem + lane_base + sb * kBN;
+      const uint32_t sa = tmem + lane_base + s_col;
       tmem_ld32(sa + 0, r0);
       tmem_ld32(sa + 32, r1);
       tmem_ld32(sa + 64, r2);
@@ -214,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       reg_fence(r2);
       reg_fence(r3);
       tc_fence_before();
-      mbar_arrive(&bars->s_free[sb]);
+      mbar_arrive(&bars->s_free[qt]);
 
       float s[128];
 #pragma unroll
@@ -230,24 +260,38 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         for (int c = 0; c < 128; ++c)
           if (c >= kv_valid) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // Row max with eight independent chains.
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const float corr = ex2_approx(m_run - m_new);
-      float rs = 0.f;
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, -m_new));
-        rs += s[c];
+      for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_cand = fmaxf(m_run, mx * sl2);
+      const bool need = m_cand > m_run + kRescaleLog2;   // always true while m_run = −∞
+      const float m_new = need ? m_cand : m_run;
+      const float corr = need ? ex2_approx(m_run - m_new) : 1.f;
+      float rs8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          s[c + i] = ex2_approx(fmaf(s[c + i], sl2, -m_new));
+          rs8[i] += s[c + i];
+        }
+      }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       l_run = l_run * corr + rs;
 
-      if (j >= 1) {
-        ok = mbar_wait(&bars->o_done, (j - 1) & 1, abort_flag, p.err, site(9));
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-      // P̃ → shared memory, bf16, 128-byte-swizzled K-major rows.
+      // P̃_i and O_i are free once the P̃_i V MMA of tile j−1 has finished.
+      ok = mbar_wait(&bars->p_free[qt], (j & 1) ^ 1, abort_flag, p.err, site(9));
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
       for (int c8 = 0; c8 < 16; ++c8) {
         uint4 v;
@@ -257,15 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         v.w = pack_bf16x2(s[8 * c8 + 6], s[8 * c8 + 7]);
         const int kb = c8 >> 3;
         const int cc = c8 & 7;
-        *reinterpret_cast<uint4*>(sP + kb * kTileBytes + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(pbuf + kb * kTileBytes + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
       }
-      // Rescale the running output when any row of this warp saw a new max.
-      if (j >= 1 && __any_sync(0xffffffffu, corr < 1.f)) {
+      // Rescale the running output only when some row of this warp moved its
+      // reference max.
+      if (j >= 1 && __any_sync(0xffffffffu, need)) {
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
-          const uint32_t oa = tmem + lane_base + kColO + c * 32;
+          const uint32_t oa = tmem + lane_base + o_col + c * 32;
           tmem_ld32(oa, r);
           tmem_wait_ld();
           reg_fence(r);
@@ -277,21 +322,21 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(&bars->p_full[qt]);
       m_run = m_new;
     }
     if (ok) {
-      ok = mbar_wait(&bars->o_done, (T - 1) & 1, abort_flag, p.err, site(10));
+      ok = mbar_wait(&bars->p_free[qt], (T - 1) & 1, abort_flag, p.err, site(10));
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         const float inv = 1.f / l_run;
-        const int grow = m0 + row;
+        const int grow = m0 + qt * kBM + row;
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + b * p.o_sb + h * p.o_sh +
                               static_cast<int64_t>(grow) * p.o_sn;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_base + kColO + c * 32, r);
+          tmem_ld32(tmem + lane_base + o_col + c * 32, r);
           tmem_wait_ld();
           reg_fence(r);
           if (grow < p.Nq) {
@@ -325,7 +370,7 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<D>;
   cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.Nq + kBM - 1) / kBM, p.H, p.B);
+  dim3 grid((p.Nq + kQT * kBM - 1) / (kQT * kBM), p.H, p.B);
   fwd_bf16_kernel<D><<<grid, kThreads, L::kSmem, stream>>>(p);
   return cudaGetLastError();
 }

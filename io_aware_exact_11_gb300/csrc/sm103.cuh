@@ -54,12 +54,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity to complete.  Returns
-// false (without completing) if the CTA's abort flag or the global error word
-// is raised meanwhile, or after kWaitTimeoutNs; on timeout it records `code`.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                       unsigned int* err, unsigned int code) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: keeps polling, bounded by kWaitTimeoutNs.  Kept out
+// of line so the common case costs one try_wait and no call.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   unsigned int* err, unsigned int code) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -76,6 +74,17 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, vo
       }
     }
   }
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Returns
+// false (without completing) if the CTA's abort flag or the global error word
+// is raised meanwhile, or after kWaitTimeoutNs; on timeout it records `code`.
+// try_wait itself suspends the thread for a while, so the first attempt
+// normally succeeds and the out-of-line loop is rarely entered.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* err, unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, code);
 }
 
 // Bounded wait used only while tearing down after an abort: ignores the flags.
