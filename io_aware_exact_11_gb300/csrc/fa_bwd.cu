@@ -12,14 +12,24 @@
 // Kernel 2: one CTA per 128-key tile K_j, V_j of one (b, h); it loops over all
 // 128-row query tiles i and accumulates dK_j, dV_j in TMEM.  Per tile, five MMAs
 // run on the tensor cores, all transposed so the key tile is the M side:
-//   Sᵀ = K_j Q_iᵀ, dPᵀ = V_j dO_iᵀ, dV += Pᵀ dO_i, dK += dSᵀ Q_i, dQ_i = dS K_j.
+//   Sᵀ = K_j Q_iᵀ, dPᵀ = V_j dO_iᵀ, dV += Pᵀ dO_i, dK += dSᵀ Q_i, dQ_iᵀ = K_jᵀ dSᵀ.
+// Pᵀ is written back into TMEM over Sᵀ (bf16 pairs) and feeds dV with A read
+// from TMEM; dSᵀ goes to shared memory, where it is the K-major A of dK and,
+// read MN-major, the A of dQ.  Q_i and dO_i are double-buffered, and the MMA
+// warp issues Sᵀ_{i+1} before dK_i and dQ_i, so the compute warps start the
+// next tile's exponentials while the tensor cores finish the current one:
+//   tensor order: Sᵀ_0 dPᵀ_0 dV_0 Sᵀ_1 dK_0 dQ_0 dPᵀ_1 dV_1 Sᵀ_2 dK_1 dQ_1 …
 // dQ_i is added into an fp32 accumulator in global memory (kernel 3 scales it
-// by σ and converts it to bf16).
+// by σ and converts it to bf16).  It is computed transposed (both operands read
+// MN-major from the K_j and dSᵀ tiles) so that TMEM lane = head-dim index: a
+// warp then adds 32 consecutive head-dim values of one query row, one full
+// 128-byte line per reduction instruction.
 //
 // Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner + MMA issuer;
 // warps 2..5 compute Pᵀ and dSᵀ (thread = key row) and write dK/dV at the end;
-// warps 6..9 drain dQ_i from TMEM (thread = query row) into the accumulator.
-// TMEM columns: Sᵀ 0..127, dPᵀ (then dQ_i) 128..255, dV 256..383, dK 384..511.
+// warps 6..9 drain dQ_iᵀ from TMEM (thread = head-dim index) into the accumulator.
+// TMEM columns: Sᵀ (then Pᵀ in 0..63) 0..127, dPᵀ (then dQ_iᵀ) 128..255,
+// dV 256..383, dK 384..511.
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -36,21 +46,23 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kOpBytes;
-constexpr int kOffQ = kOffV + kOpBytes;
-constexpr int kOffDO = kOffQ + kOpBytes;
-constexpr int kOffPT = kOffDO + kOpBytes;
-constexpr int kOffDST = kOffPT + kOpBytes;
-constexpr int kOffStats = kOffDST + kOpBytes;      // lse2[2][128], delta[2][128]
-constexpr int kOffBar = kOffStats + 4 * 128 * 4;
-constexpr int kSmem = kOffBar + 512 + 1024;
+constexpr int kOffQ = kOffV + kOpBytes;       // two buffers
+constexpr int kOffDO = kOffQ + 2 * kOpBytes;  // two buffers
+constexpr int kOffDST = kOffDO + 2 * kOpBytes;
+constexpr int kOffStats = kOffDST + kOpBytes;  // lse2[128], delta[128]
+constexpr int kOffBar = kOffStats + 2 * 128 * 4;
+constexpr int kSmem = kOffBar + 256 + 1024;
+static_assert(kSmem <= 232448, "shared memory budget");
 
 struct BwdBars {
-  uint64_t kv_full, qdo_full, qdo_empty;
-  uint64_t s_full, s_free, dp_full, dq_full, dq_free;
-  uint64_t p_ready, ds_ready, ps_free, acc_done, drain;
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, dp_full, dq_full, dq_free;
+  uint64_t p_ready, ds_ready, ds_free, acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernBwd << 8) | s; }
 
@@ -112,14 +124,17 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   }
 }
 
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
 // ---------------------------------------------------------------- kernel 2
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + kOffBar);
-  float* s_lse = reinterpret_cast<float*>(smem + kOffStats);   // [2][128]
-  float* s_del = s_lse + 2 * 128;                              // [2][128]
+  float* s_lse = reinterpret_cast<float*>(smem + kOffStats);   // [128]
+  float* s_del = s_lse + 128;                                  // [128]
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -132,16 +147,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
-    mbar_init(&bars->qdo_full, 1);
-    mbar_init(&bars->qdo_empty, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&bars->q_full[q], 1);
+      mbar_init(&bars->q_empty[q], 1);
+    }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 128);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->p_ready, 128);
     mbar_init(&bars->ds_ready, 128);
-    mbar_init(&bars->ps_free, 1);
+    mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -170,73 +186,90 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       }
       int issued = 0;
       for (int i = 0; i < T; ++i) {
-        if (!mbar_wait(&bars->qdo_empty, (i & 1) ^ 1, abort_flag, p.err, site(1))) break;
-        mbar_arrive_expect_tx(&bars->qdo_full, 2 * kOpBytes);
+        const int qb = i & 1;
+        if (!mbar_wait(&bars->q_empty[qb], ((i >> 1) & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        mbar_arrive_expect_tx(&bars->q_full[qb], 2 * kOpBytes);
         for (int kb = 0; kb < 2; ++kb) {
-          tma_load_4d(smem + kOffQ + kb * kTileBytes, &p.tm_q, &bars->qdo_full, kb * 64, i * kTile, h, b);
-          tma_load_4d(smem + kOffDO + kb * kTileBytes, &p.tm_do, &bars->qdo_full, kb * 64, i * kTile, h, b);
+          tma_load_4d(smem + kOffQ + qb * kOpBytes + kb * kTileBytes, &p.tm_q, &bars->q_full[qb], kb * 64,
+                      i * kTile, h, b);
+          tma_load_4d(smem + kOffDO + qb * kOpBytes + kb * kTileBytes, &p.tm_do, &bars->q_full[qb], kb * 64,
+                      i * kTile, h, b);
         }
         ++issued;
       }
       if (*abort_flag) {
         mbar_wait_drain(&bars->kv_full, 0, 200000000ull);
-        if (issued > 0) mbar_wait_drain(&bars->qdo_full, (issued - 1) & 1, 200000000ull);
+        for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
+          mbar_wait_drain(&bars->q_full[t & 1], (t >> 1) & 1, 200000000ull);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // Sᵀ, dPᵀ
-      constexpr uint32_t kIdescKM = idesc_bf16_f32(128, kD, false, true);    // dV, dK
+      constexpr uint32_t kIdescKM = idesc_bf16_f32(128, kD, false, true);    // dV (A in TMEM), dK
       constexpr uint32_t kIdescMM = idesc_bf16_f32(128, kD, true, true);     // dQ
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sQ = smem_u32(smem + kOffQ), sDO = smem_u32(smem + kOffDO);
-      const uint32_t sPT = smem_u32(smem + kOffPT), sDST = smem_u32(smem + kOffDST);
-      bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, site(2));
-      for (int i = 0; ok && i < T; ++i) {
-        const uint32_t ph = i & 1;
-        ok = mbar_wait(&bars->qdo_full, ph, abort_flag, p.err, site(3)) &&
-             mbar_wait(&bars->s_free, ph ^ 1, abort_flag, p.err, site(4));
-        if (!ok) break;
-        tc_fence_after();
+      const uint32_t sDST = smem_u32(smem + kOffDST);
+      auto issue_st = [&](int i) {  // Sᵀ = K_j Q_iᵀ
+        const uint32_t q = sQ + (i & 1) * kOpBytes;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {  // Sᵀ = K_j Q_iᵀ
+        for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), kIdescKK,
+          mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024), kIdescKK,
                       kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full);
-        if (!(ok = mbar_wait(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(5)))) break;
+      };
+      bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, site(2)) &&
+                mbar_wait(&bars->q_full[0], 0, abort_flag, p.err, site(3));
+      if (ok) {
+        tc_fence_after();
+        issue_st(0);
+      }
+      for (int i = 0; ok && i < T; ++i) {
+        const uint32_t ph = i & 1;
+        const uint32_t dob = sDO + (i & 1) * kOpBytes;
+        const uint32_t qb = sQ + (i & 1) * kOpBytes;
+        // dPᵀ_i = V_j dO_iᵀ into columns that held dQ_{i−1}: wait until it is drained.
+        if (!(ok = mbar_wait(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(4)))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {  // dPᵀ = V_j dO_iᵀ
+        for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), kIdescKK,
+          mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), kIdescKK,
                       kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dp_full);
-        if (!(ok = mbar_wait(&bars->p_ready, ph, abort_flag, p.err, site(6)))) break;
+        // dV += Pᵀ dO_i with Pᵀ (bf16 pairs) read from TMEM columns 0..63.
+        if (!(ok = mbar_wait(&bars->p_ready, ph, abort_flag, p.err, site(5)))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {  // dV += Pᵀ dO_i
-          mma_bf16_ss(tmem + kColDV, sdesc_sw128(sPT + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
-                      sdesc_sw128(sDO + kk * 2048, kTileBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tmem + kColDV, tmem + kColS + kk * 8, sdesc_sw128(dob + kk * 2048, kTileBytes, 1024), kIdescKM,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+        // Sᵀ_{i+1} overwrites Pᵀ_i, which the dV MMAs above read first (in order).
+        if (i + 1 < T) {
+          if (!(ok = mbar_wait(&bars->q_full[(i + 1) & 1], ((i + 1) >> 1) & 1, abort_flag, p.err, site(6)))) break;
+          tc_fence_after();
+          issue_st(i + 1);
         }
         if (!(ok = mbar_wait(&bars->ds_ready, ph, abort_flag, p.err, site(7)))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {  // dK += dSᵀ Q_i
           mma_bf16_ss(tmem + kColDK, sdesc_sw128(sDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
-                      sdesc_sw128(sQ + kk * 2048, kTileBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+                      sdesc_sw128(qb + kk * 2048, kTileBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {  // dQ_i = dS K_j (dS read MN-major from dSᵀ)
-          mma_bf16_ss(tmem + kColDP, sdesc_sw128(sDST + kk * 2048, kTileBytes, 1024),
-                      sdesc_sw128(sK + kk * 2048, kTileBytes, 1024), kIdescMM, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kTile / 16; ++kk) {  // dQ_iᵀ = K_jᵀ dSᵀ (A = K_j and B = dSᵀ, both MN-major)
+          mma_bf16_ss(tmem + kColDP, sdesc_sw128(sK + kk * 2048, kTileBytes, 1024),
+                      sdesc_sw128(sDST + kk * 2048, kTileBytes, 1024), kIdescMM, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->qdo_empty);
-        mma_commit(&bars->ps_free);
+        mma_commit(&bars->ds_free);
+        mma_commit(&bars->q_empty[i & 1]);
       }
       mma_commit(&bars->acc_done);
       if (*abort_flag) {
@@ -251,56 +284,59 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     const int tr = threadIdx.x - 64;          // 0..127, for staging row stats
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint8_t* sPT = smem + kOffPT;
     uint8_t* sDST = smem + kOffDST;
+    // The named barriers below are reached on every iteration by all four
+    // warps; after an abort a warp keeps iterating without doing work, so no
+    // warp is ever left waiting at a barrier another warp has abandoned.
     bool ok = true;
     for (int i = 0; i < T; ++i) {
       const uint32_t ph = i & 1;
-      float* lse_t = s_lse + ph * 128;
-      float* del_t = s_del + ph * 128;
-      lse_t[tr] = p.lse_log2[bh * p.N + i * kTile + tr];
-      del_t[tr] = p.delta[bh * p.N + i * kTile + tr];
+      named_sync(1, 128);  // every thread is done reading the previous tile's stats
+      s_lse[tr] = p.lse_log2[bh * p.N + i * kTile + tr];
+      s_del[tr] = p.delta[bh * p.N + i * kTile + tr];
       named_sync(1, 128);
+      if (!ok) continue;
 
       ok = mbar_wait(&bars->s_full, ph, abort_flag, p.err, site(8));
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; continue; }
       tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tmem + lane_base + kColS + 0, r0);
-      tmem_ld32(tmem + lane_base + kColS + 32, r1);
-      tmem_ld32(tmem + lane_base + kColS + 64, r2);
-      tmem_ld32(tmem + lane_base + kColS + 96, r3);
-      tmem_wait_ld();
-      reg_fence(r0);
-      reg_fence(r1);
-      reg_fence(r2);
-      reg_fence(r3);
+      // Pᵀ row = e^(σ Sᵀ row − LSE) as bf16 pairs, written back over Sᵀ (columns 0..63).
+      uint32_t pk[64];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tmem + lane_base + kColS + half * 64, ra);
+        tmem_ld32(tmem + lane_base + kColS + half * 64 + 32, rb);
+        tmem_wait_ld();
+        reg_fence(ra);
+        reg_fence(rb);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = half * 64 + 2 * e;
+          pk[half * 32 + e] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(ra[2 * e]), sl2, -s_lse[c])),
+                                          ex2_approx(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -s_lse[c + 1])));
+          pk[half * 32 + 16 + e] =
+              pack_bf16x2(ex2_approx(fmaf(__uint_as_float(rb[2 * e]), sl2, -s_lse[c + 32])),
+                          ex2_approx(fmaf(__uint_as_float(rb[2 * e + 1]), sl2, -s_lse[c + 33])));
+        }
+      }
+      {
+        uint32_t w0[32], w1[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          w0[e] = pk[e];
+          w1[e] = pk[32 + e];
+        }
+        tmem_st32(tmem + lane_base + kColS, w0);
+        tmem_st32(tmem + lane_base + kColS + 32, w1);
+        tmem_wait_st();
+      }
       tc_fence_before();
-      mbar_arrive(&bars->s_free);
-      float pv[128];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        pv[c] = ex2_approx(fmaf(__uint_as_float(r0[c]), sl2, -lse_t[c]));
-        pv[32 + c] = ex2_approx(fmaf(__uint_as_float(r1[c]), sl2, -lse_t[32 + c]));
-        pv[64 + c] = ex2_approx(fmaf(__uint_as_float(r2[c]), sl2, -lse_t[64 + c]));
-        pv[96 + c] = ex2_approx(fmaf(__uint_as_float(r3[c]), sl2, -lse_t[96 + c]));
-      }
-      ok = mbar_wait(&bars->ps_free, ph ^ 1, abort_flag, p.err, site(9));
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint4 v;
-        v.x = pack_bf16x2(pv[8 * c8 + 0], pv[8 * c8 + 1]);
-        v.y = pack_bf16x2(pv[8 * c8 + 2], pv[8 * c8 + 3]);
-        v.z = pack_bf16x2(pv[8 * c8 + 4], pv[8 * c8 + 5]);
-        v.w = pack_bf16x2(pv[8 * c8 + 6], pv[8 * c8 + 7]);
-        *reinterpret_cast<uint4*>(sPT + (c8 >> 3) * kTileBytes + r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = v;
-      }
-      fence_proxy_async_smem();
       mbar_arrive(&bars->p_ready);
 
-      ok = mbar_wait(&bars->dp_full, ph, abort_flag, p.err, site(10));
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ok = mbar_wait(&bars->dp_full, ph, abort_flag, p.err, site(9)) &&
+           mbar_wait(&bars->ds_free, ph ^ 1, abort_flag, p.err, site(10));
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; continue; }
       tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -310,19 +346,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         reg_fence(rd);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          float ds[8];
+          uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int c = cc * 32 + q4 * 8 + e;
-            ds[e] = pv[c] * (__uint_as_float(rd[q4 * 8 + e]) - del_t[c]);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int c = cc * 32 + q4 * 8 + 2 * e2;           // query column
+            const uint32_t pw = pk[c >> 1];
+            const float d0 = bf16lo(pw) * (__uint_as_float(rd[q4 * 8 + 2 * e2]) - s_del[c]);
+            const float d1 = bf16hi(pw) * (__uint_as_float(rd[q4 * 8 + 2 * e2 + 1]) - s_del[c + 1]);
+            w[e2] = pack_bf16x2(d0, d1);
           }
-          uint4 v;
-          v.x = pack_bf16x2(ds[0], ds[1]);
-          v.y = pack_bf16x2(ds[2], ds[3]);
-          v.z = pack_bf16x2(ds[4], ds[5]);
-          v.w = pack_bf16x2(ds[6], ds[7]);
           const int c8 = cc * 4 + q4;
-          *reinterpret_cast<uint4*>(sDST + (c8 >> 3) * kTileBytes + r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(sDST + (c8 >> 3) * kTileBytes + r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
@@ -355,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       }
     }
   } else {
-    // ------------------------------------------------------ dQ_i drain
+    // ------------------------------------------------------ dQ_iᵀ drain
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // query row within the tile
+    const int dcol = wq * 32 + lane;  // head-dim index (TMEM lane)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     for (int i = 0; i < T; ++i) {
       const bool ok = mbar_wait(&bars->dq_full, i & 1, abort_flag, p.err, site(12));
@@ -375,17 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       reg_fence(r3);
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
-      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile + r) * kD);
+      // Column c of dQ_iᵀ is query row i·128 + c; lanes cover consecutive head dims.
+      float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * kD + dcol;
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        atomicAdd(dst + c4, make_float4(__uint_as_float(r0[4 * c4]), __uint_as_float(r0[4 * c4 + 1]),
-                                        __uint_as_float(r0[4 * c4 + 2]), __uint_as_float(r0[4 * c4 + 3])));
-        atomicAdd(dst + 8 + c4, make_float4(__uint_as_float(r1[4 * c4]), __uint_as_float(r1[4 * c4 + 1]),
-                                            __uint_as_float(r1[4 * c4 + 2]), __uint_as_float(r1[4 * c4 + 3])));
-        atomicAdd(dst + 16 + c4, make_float4(__uint_as_float(r2[4 * c4]), __uint_as_float(r2[4 * c4 + 1]),
-                                             __uint_as_float(r2[4 * c4 + 2]), __uint_as_float(r2[4 * c4 + 3])));
-        atomicAdd(dst + 24 + c4, make_float4(__uint_as_float(r3[4 * c4]), __uint_as_float(r3[4 * c4 + 1]),
-                                             __uint_as_float(r3[4 * c4 + 2]), __uint_as_float(r3[4 * c4 + 3])));
+      for (int c = 0; c < 32; ++c) {
+        atomicAdd(dst + (c + 0) * kD, __uint_as_float(r0[c]));
+        atomicAdd(dst + (c + 32) * kD, __uint_as_float(r1[c]));
+        atomicAdd(dst + (c + 64) * kD, __uint_as_float(r2[c]));
+        atomicAdd(dst + (c + 96) * kD, __uint_as_float(r3[c]));
       }
     }
   }
