@@ -44,7 +44,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/fwd_bf16_kernel_prefill_B4_H32_N4096_d128.md
-    "fwd_prefill": {"src": "106cb2c15a862360", "bytes": 402754560 + 117957888},
+    "fwd_prefill": {"src": "745faee6a3509062", "bytes": 402710272 + 117554944},
+    # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
+    "bwd_train": {"src": "57502e753943cca5", "bytes": 405177856 + 230648576},
+    # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
+    # proportional to B, stored here scaled to the B=64 launch
+    "decode_split": {"src": "901f9d8b8d4d9813", "bytes": (1073857000 + 6977280) * 8},
 }
 
 
@@ -310,10 +315,11 @@ def run_ours(args, ws, rank, local):
     del qh, kh, vh, oh, lh
 
     extra = {}
-    if not args.quick:
+    extras = set() if args.quick else {x for x in args.extras.split(",") if x}
+    del q, k, v, o, lse
+    if "long" in extras:
         # ---------------- long-context forward
         Bl, Hl, Nl = LONG["B"], LONG["H"], LONG["N"]
-        del q, k, v, o, lse
         ql, kl, vl = randn((Bl, Hl, Nl, d), 4), randn((Bl, Hl, Nl, d), 5), randn((Bl, Hl, Nl, d), 6)
         ol = torch.empty_like(ql)
         ll = torch.empty((Bl, Hl, Nl), dtype=torch.float32, device=dev)
@@ -324,8 +330,9 @@ def run_ours(args, ws, rank, local):
                                  "ms": t_long * 1e3, "frac_of_bf16_peak": fl / t_long / 1e12 / peak}
         del ql, kl, vl, ol, ll
 
+    if "decode" in extras:
         # ---------------- decode
-        Bd, Hd, Nd, S = DECODE["B"], DECODE["H"], DECODE["N"], DECODE["splits"]
+        Bd, Hd, Nd, S = args.decode_batch, DECODE["H"], DECODE["N"], DECODE["splits"]
         qd = randn((Bd, Hd, 1, d), 7)
         kd, vd = randn((Bd, Hd, Nd, d), 8), randn((Bd, Hd, Nd, d), 9)
         od = torch.empty_like(qd)
@@ -335,12 +342,19 @@ def run_ours(args, ws, rank, local):
         t_dec = timed(lambda: fa.decode_splitkv(qd, kd, vd, n_splits=S, out=od, lse=ld, workspace=ws_d),
                       n_dec, 2) / n_dec
         kv_bytes = 2.0 * Bd * Hd * Nd * d * 2
-        extra["decode"] = {"workload": "B=64 H=32 S_q=1 N_kv=8192 d=128 bf16, 32 splits",
+        dec_traffic = traffic_for("decode_split", ("fa_decode.cu", "sm103.cuh"))
+        extra["decode"] = {"workload": f"B={Bd} H=32 S_q=1 N_kv=8192 d=128 bf16, 32 splits",
                            "hbm_gbs": kv_bytes / t_dec / 1e9, "tokens_per_s": Bd / t_dec, "ms": t_dec * 1e3,
                            "frac_of_hbm_peak": kv_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"]),
-                           "bytes_per_step": kv_bytes}
+                           "bytes_per_step": kv_bytes,
+                           "roofline": {"bound": "hbm", "achieved": kv_bytes / t_dec / 1e9,
+                                        "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                                        "frac": kv_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"]),
+                                        "kernel": "decode_split_kernel + decode_merge_kernel",
+                                        "traffic": None if dec_traffic is None else dec_traffic * Bd / 64}}
         del qd, kd, vd, od, ld, ws_d
 
+    if "train" in extras:
         # ---------------- training forward + backward
         Bt, Ht, Nt = TRAIN["B"], TRAIN["H"], TRAIN["N"]
         qt, kt, vt, dot = (randn((Bt, Ht, Nt, d), s) for s in (10, 11, 12, 13))
@@ -356,8 +370,12 @@ def run_ours(args, ws, rank, local):
         extra["train"] = {"workload": "B=2 H=16 N=8192 d=128 bf16", "fwd_tflops": ff / t_f / 1e12,
                           "bwd_tflops": 2.5 * ff / t_b / 1e12, "fwd_ms": t_f * 1e3, "bwd_ms": t_b * 1e3,
                           "fwd_frac_of_bf16_peak": ff / t_f / 1e12 / peak,
-                          "bwd_frac_of_bf16_peak": 2.5 * ff / t_b / 1e12 / peak}
-        fa.device_status()
+                          "bwd_frac_of_bf16_peak": 2.5 * ff / t_b / 1e12 / peak,
+                          "bwd_roofline": {"bound": "tensor", "achieved": 2.5 * ff / t_b / 1e12, "peak": peak,
+                                           "unit": "TFLOP/s", "frac": 2.5 * ff / t_b / 1e12 / peak,
+                                           "kernel": "time: whole backward (3 kernels); traffic: bwd_main_kernel",
+                                           "traffic": traffic_for("bwd_train", ("fa_bwd.cu", "sm103.cuh"))}}
+    fa.device_status()
 
     if rank != 0:
         return
@@ -394,6 +412,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
+    ap.add_argument("--extras", default="long,decode,train",
+                    help="comma list of extra workloads measured after the headline")
+    ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
+                    help="decode batch B (64 is the configured workload; smaller only for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
