@@ -10,6 +10,7 @@ from .attention import (  # noqa: F401
     attention_probs,
     attention_rows,
     backward_delta,
+    causal_visible,
     merge_partials,
     online_attention,
     scores,

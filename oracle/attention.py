@@ -31,6 +31,10 @@ Every function computes in float64.  What each one follows:
   oracle for the kernels.
 * ``split_partials`` / ``merge_partials``: unnormalised per-chunk triples
   (m_c, ℓ_c, o_c) and the block-merge rule of [Notes] §二.3.
+* ``causal=True`` (forward, rows, backward): the causal mask of the lesson's
+  memory lab (§5, ``is_causal=True``), bottom-right aligned: query i of Nq
+  sees keys j <= i + (Nk − Nq).  Masked scores are −∞ before the softmax,
+  the plain definition with those entries removed.
 * ``attention_backward``: the pages give no gradient formulas, only that the
   backward recomputes S and P from Q, K, V and the saved statistics
   ([Walk] "Flash Attention Backward", [Notes] §二.5).  The oracle uses the
@@ -47,6 +51,7 @@ import numpy as np
 
 __all__ = [
     "scores",
+    "causal_visible",
     "attention_probs",
     "attention_forward",
     "attention_rows",
@@ -69,6 +74,18 @@ def scores(q, k, scale: float) -> np.ndarray:
     return float(scale) * (q @ k.T)
 
 
+def causal_visible(rows, nq: int, nk: int) -> np.ndarray:
+    """Boolean [len(rows), nk]: key j is visible to query row i when j <= i + nk − nq."""
+    rows = np.asarray(rows, dtype=np.int64)
+    return np.arange(nk)[None, :] <= (rows[:, None] + (nk - nq))
+
+
+def _mask(s, rows, nq, nk, causal):
+    if not causal:
+        return s
+    return np.where(causal_visible(rows, nq, nk), s, -np.inf)
+
+
 def _softmax_rows(s: np.ndarray):
     """Row softmax with the row max subtracted ([Walk] "Safe Softmax").
 
@@ -80,27 +97,30 @@ def _softmax_rows(s: np.ndarray):
     return e / l[:, None], m, l
 
 
-def attention_probs(q, k, scale: float) -> np.ndarray:
+def attention_probs(q, k, scale: float, causal: bool = False) -> np.ndarray:
     """P = softmax(σ·QKᵀ) for 2-D inputs, fully materialised."""
-    p, _, _ = _softmax_rows(scores(q, k, scale))
+    nq, nk = q.shape[0], k.shape[0]
+    p, _, _ = _softmax_rows(_mask(scores(q, k, scale), np.arange(nq), nq, nk, causal))
     return p
 
 
-def _head_forward(q, k, v, scale, row_block):
+def _head_forward(q, k, v, scale, row_block, causal=False, rows=None, nq_total=None):
     nq = q.shape[0]
+    rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
+    nq_total = nq if nq_total is None else nq_total
     o = np.empty((nq, v.shape[1]), dtype=np.float64)
     lse = np.empty((nq,), dtype=np.float64)
     step = nq if row_block is None else int(row_block)
     for r0 in range(0, nq, step):
         r1 = min(nq, r0 + step)
-        s = scores(q[r0:r1], k, scale)
+        s = _mask(scores(q[r0:r1], k, scale), rows[r0:r1], nq_total, k.shape[0], causal)
         p, m, l = _softmax_rows(s)
         o[r0:r1] = p @ v
         lse[r0:r1] = m + np.log(l)
     return o, lse
 
 
-def attention_forward(q, k, v, scale: float, row_block: int | None = 256):
+def attention_forward(q, k, v, scale: float, row_block: int | None = 256, causal: bool = False):
     """Exact attention, materialised one block of query rows at a time.
 
     q: [..., Nq, d], k and v: [..., Nk, d] (any leading batch dims, e.g. B, H).
@@ -120,12 +140,14 @@ def attention_forward(q, k, v, scale: float, row_block: int | None = 256):
     vf = v.reshape((-1,) + v.shape[-2:])
     o = np.empty(qf.shape[:-1] + (vf.shape[-1],), dtype=np.float64)
     lse = np.empty(qf.shape[:-1], dtype=np.float64)
+    if causal:
+        assert q.shape[-2] <= k.shape[-2], "causal attention needs Nq <= Nk"
     for g in range(qf.shape[0]):
-        o[g], lse[g] = _head_forward(qf[g], kf[g], vf[g], scale, row_block)
+        o[g], lse[g] = _head_forward(qf[g], kf[g], vf[g], scale, row_block, causal)
     return o.reshape(lead + o.shape[-2:]), lse.reshape(lead + lse.shape[-1:])
 
 
-def attention_rows(q_head, k_head, v_head, scale: float, rows):
+def attention_rows(q_head, k_head, v_head, scale: float, rows, causal: bool = False):
     """Exact attention for selected query rows of one head.
 
     q_head [Nq, d], k_head/v_head [Nk, d]; ``rows`` indexes q_head.  Rows are
@@ -134,7 +156,7 @@ def attention_rows(q_head, k_head, v_head, scale: float, rows):
     """
     rows = np.asarray(rows, dtype=np.int64)
     q = _f64(q_head)[rows]
-    return _head_forward(q, _f64(k_head), _f64(v_head), scale, None)
+    return _head_forward(q, _f64(k_head), _f64(v_head), scale, None, causal, rows, q_head.shape[0])
 
 
 def online_attention(q, k, v, scale: float, block: int):
@@ -226,8 +248,8 @@ def backward_delta(do, o) -> np.ndarray:
     return np.sum(_f64(do) * _f64(o), axis=-1)
 
 
-def _head_backward(q, k, v, do, scale):
-    p = attention_probs(q, k, scale)          # recomputed, never stored by the kernels
+def _head_backward(q, k, v, do, scale, causal=False):
+    p = attention_probs(q, k, scale, causal)  # recomputed, never stored by the kernels
     o = p @ v
     dv = p.T @ do                             # O = P V  ⇒  dV = Pᵀ dO
     dp = do @ v.T                             #            dP = dO Vᵀ
@@ -238,12 +260,14 @@ def _head_backward(q, k, v, do, scale):
     return dq, dk, dv, o
 
 
-def attention_backward(q, k, v, do, scale: float):
+def attention_backward(q, k, v, do, scale: float, causal: bool = False):
     """Gradients of O = softmax(σ·QKᵀ)·V with respect to Q, K, V.
 
     q/k/v/do: [..., N, d].  The textbook derivation: dV = Pᵀ·dO,
     dP = dO·Vᵀ, dS = P ∘ (dP − rowsum(P ∘ dP)), dQ = σ·dS·K, dK = σ·dSᵀ·Q.
-    P is recomputed here from Q and K.  Returns (dQ, dK, dV) in float64.
+    P is recomputed here from Q and K (with the causal mask when ``causal``:
+    masked entries of P are 0, so they drop out of every product).  Returns
+    (dQ, dK, dV) in float64.
     """
     q = _f64(q)
     k = _f64(k)
@@ -258,5 +282,5 @@ def attention_backward(q, k, v, do, scale: float):
     dk = np.empty_like(kf)
     dv = np.empty_like(vf)
     for g in range(qf.shape[0]):
-        dq[g], dk[g], dv[g], _ = _head_backward(qf[g], kf[g], vf[g], dof[g], scale)
+        dq[g], dk[g], dv[g], _ = _head_backward(qf[g], kf[g], vf[g], dof[g], scale, causal)
     return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)

@@ -268,3 +268,75 @@ def test_backward_matches_torch_autograd_fp64():
     assert np.allclose(tq.grad.numpy(), dq, atol=1e-12)
     assert np.allclose(tk.grad.numpy(), dk, atol=1e-12)
     assert np.allclose(tv.grad.numpy(), dv, atol=1e-12)
+
+
+# ------------------------------------------------------------------ causal
+# The causal mask follows the lesson's memory lab (§5, is_causal=True),
+# bottom-right aligned: query i of Nq sees keys j <= i + Nk − Nq.
+
+
+@pytest.mark.parametrize("nq,nk", [(9, 9), (5, 12), (1, 7), (16, 16)])
+def test_causal_row_equals_unmasked_attention_over_its_prefix(nq, nk):
+    """Independent route: the masked row is the plain definition on a truncated key set."""
+    q = RNG.standard_normal((nq, 6))
+    k = RNG.standard_normal((nk, 6))
+    v = RNG.standard_normal((nk, 6))
+    o, lse = oracle.attention_forward(q, k, v, 0.4, causal=True)
+    for i in range(nq):
+        n_vis = i + (nk - nq) + 1
+        oi, li = oracle.attention_forward(q[i:i + 1], k[:n_vis], v[:n_vis], 0.4)
+        assert np.allclose(o[i], oi[0], atol=1e-14)
+        assert abs(lse[i] - li[0]) < 1e-13
+        s = 0.4 * (k[:n_vis] @ q[i])
+        assert abs(lse[i] - special.logsumexp(s)) < 1e-13
+
+
+def test_causal_first_and_last_rows():
+    n = 10
+    q = RNG.standard_normal((n, 4))
+    k = RNG.standard_normal((n, 4))
+    v = RNG.standard_normal((n, 4))
+    o, lse = oracle.attention_forward(q, k, v, 0.5, causal=True)
+    full_o, full_lse = oracle.attention_forward(q, k, v, 0.5)
+    assert np.allclose(o[0], v[0], atol=1e-15)            # row 0 sees key 0 only
+    assert abs(lse[0] - 0.5 * q[0] @ k[0]) < 1e-15
+    assert np.allclose(o[-1], full_o[-1], atol=1e-15)     # the last row sees every key
+    assert abs(lse[-1] - full_lse[-1]) < 1e-15
+
+
+def test_causal_rows_helper_and_row_blocks_agree():
+    q = RNG.standard_normal((2, 2, 40, 8))
+    k = RNG.standard_normal((2, 2, 55, 8))
+    v = RNG.standard_normal((2, 2, 55, 8))
+    ref = oracle.attention_forward(q, k, v, 0.3, row_block=None, causal=True)
+    o, lse = oracle.attention_forward(q, k, v, 0.3, row_block=7, causal=True)
+    assert np.max(np.abs(o - ref[0])) <= 1e-13
+    rows = [0, 13, 39]
+    o2, l2 = oracle.attention_rows(q[1, 0], k[1, 0], v[1, 0], 0.3, rows, causal=True)
+    assert np.max(np.abs(o2 - ref[0][1, 0][rows])) <= 1e-14
+    assert np.max(np.abs(l2 - ref[1][1, 0][rows])) <= 1e-14
+
+
+def test_causal_backward_matches_finite_differences():
+    rng = np.random.default_rng(77)
+    n, d = 6, 3
+    q, k, v, do = (rng.standard_normal((n, d)) for _ in range(4))
+    scale = 0.6
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, scale, causal=True)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_forward(qq, kk, vv, scale, causal=True)
+        return float(np.sum(o * do))
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            args = {"q": q, "k": k, "v": v}
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            num[idx] = (loss(**{**{"qq": q, "kk": k, "vv": v}, **{name * 2: xp}})
+                        - loss(**{**{"qq": q, "kk": k, "vv": v}, **{name * 2: xm}})) / (2 * h)
+        assert np.linalg.norm(num - g) / np.linalg.norm(num) <= 1e-6, name
+    # The last key only reaches the last query row.
+    assert np.allclose(dv[-1], oracle.attention_probs(q, k, scale, True)[-1, -1] * do[-1], atol=1e-14)
