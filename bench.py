@@ -375,6 +375,35 @@ def run_ours(args, ws, rank, local):
                                            "unit": "TFLOP/s", "frac": 2.5 * ff / t_b / 1e12 / peak,
                                            "kernel": "time: whole backward (3 kernels); traffic: bwd_main_kernel",
                                            "traffic": traffic_for("bwd_train", ("fa_bwd.cu", "sm103.cuh"))}}
+    if "causal" in extras:
+        # ---------------- causal mask: prefill forward and training backward
+        Bc, Hc, Nc = PREFILL["B"], PREFILL["H"], PREFILL["N"]
+        qc, kc, vc = randn((Bc, Hc, Nc, d), 14), randn((Bc, Hc, Nc, d), 15), randn((Bc, Hc, Nc, d), 16)
+        oc = torch.empty_like(qc)
+        lc = torch.empty((Bc, Hc, Nc), dtype=torch.float32, device=dev)
+        n_c = max(5, min(args.steps, 50))
+        t_c = timed(lambda: fa.forward(qc, kc, vc, out=oc, lse=lc, causal=True), n_c, 2) / n_c
+        fc = 4.0 * Bc * Hc * d * Nc * (Nc + 1) / 2          # visible (query, key) pairs only
+        del qc, kc, vc, oc, lc
+        Bt, Ht, Nt = TRAIN["B"], TRAIN["H"], TRAIN["N"]
+        qt, kt, vt, dot = (randn((Bt, Ht, Nt, d), s) for s in (17, 18, 19, 20))
+        ot = torch.empty_like(qt)
+        lt = torch.empty((Bt, Ht, Nt), dtype=torch.float32, device=dev)
+        fa.forward(qt, kt, vt, out=ot, lse=lt, causal=True)
+        dq, dk, dv = torch.empty_like(qt), torch.empty_like(kt), torch.empty_like(vt)
+        ws_b = torch.empty(fa.backward_workspace_size(Bt, Ht, Nt, d), dtype=torch.uint8, device=dev)
+        n_tr = max(3, min(args.steps // 5, 20))
+        t_cb = timed(lambda: fa.backward(qt, kt, vt, ot, lt, dot, dq=dq, dk=dk, dv=dv, workspace=ws_b, causal=True),
+                     n_tr, 1) / n_tr
+        fcb = 2.5 * 4.0 * Bt * Ht * d * Nt * (Nt + 1) / 2
+        extra["causal"] = {"flop_count": "4·B·H·d·N(N+1)/2 (visible pairs); backward 2.5x that",
+                           "prefill_fwd": {"workload": "B=4 H=32 N=4096 d=128 bf16 causal",
+                                           "tflops": fc / t_c / 1e12, "ms": t_c * 1e3,
+                                           "frac_of_bf16_peak": fc / t_c / 1e12 / peak},
+                           "train_bwd": {"workload": "B=2 H=16 N=8192 d=128 bf16 causal",
+                                         "tflops": fcb / t_cb / 1e12, "ms": t_cb * 1e3,
+                                         "frac_of_bf16_peak": fcb / t_cb / 1e12 / peak}}
+        del qt, kt, vt, dot, ot, lt, dq, dk, dv, ws_b
     fa.device_status()
 
     if rank != 0:
@@ -412,7 +441,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
-    ap.add_argument("--extras", default="long,decode,train",
+    ap.add_argument("--extras", default="long,decode,train,causal",
                     help="comma list of extra workloads measured after the headline")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="decode batch B (64 is the configured workload; smaller only for profiling)")

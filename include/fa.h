@@ -61,6 +61,11 @@ typedef enum fa_status {
 
 typedef enum fa_dtype { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
 
+/* Attention mask.  FA_MASK_CAUSAL is the causal mask the lesson's memory lab
+ * uses (§5, is_causal=True), aligned to the bottom-right corner: query row i of
+ * N_q sees keys j <= i + (N_kv − N_q); it needs N_q <= N_kv so no row is empty. */
+typedef enum fa_mask { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 1 } fa_mask;
+
 /* Version of this ABI; bumped on any incompatible change. */
 FA_API int fa_abi_version(void);
 
@@ -81,6 +86,16 @@ FA_API int fa_abi_version(void);
 FA_API fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int H, int N_q, int N_kv, int d, fa_dtype dtype, float scale,
                      const int64_t* strides, void* stream);
+
+/*
+ * fa_forward_masked — fa_forward with a mask (FA_MASK_NONE is fa_forward).
+ *   With FA_MASK_CAUSAL masked scores are −∞ before the softmax; a CTA streams
+ *   only the key tiles its rows can see.  N_q > N_kv with a causal mask gives
+ *   FA_ERR_INVALID_ARG.  Same arguments, layouts and support as fa_forward.
+ */
+FA_API fa_status fa_forward_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                                   int B, int H, int N_q, int N_kv, int d, fa_dtype dtype, float scale,
+                                   const int64_t* strides, fa_mask mask, void* stream);
 
 /*
  * fa_decode_workspace_size — bytes of workspace fa_decode_splitkv needs:
@@ -159,6 +174,17 @@ FA_API fa_status fa_backward(const void* q, const void* k, const void* v, const 
                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                       fa_dtype dtype, float scale, void* workspace, size_t workspace_bytes,
                       void* stream);
+
+/*
+ * fa_backward_masked — fa_backward for a forward run with `mask` (FA_MASK_NONE
+ *   is fa_backward).  With FA_MASK_CAUSAL (query i sees key j <= i) each key
+ *   tile only visits the query tiles at or after its diagonal.  Same arguments,
+ *   workspace and support as fa_backward.
+ */
+FA_API fa_status fa_backward_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                    fa_dtype dtype, float scale, void* workspace, size_t workspace_bytes,
+                                    fa_mask mask, void* stream);
 
 /*
  * fa_device_status — synchronises `stream`, then reports FA_ERR_DEVICE_TIMEOUT

@@ -133,8 +133,13 @@ const char* fa_get_last_error(void) { return g_last_error; }
 
 uint64_t fa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
-                     int N_kv, int d, fa_dtype dtype, float scale, const int64_t* strides, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                       int N_kv, int d, fa_dtype dtype, float scale, const int64_t* strides, int causal,
+                       void* stream) {
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_forward: null tensor pointer");
   if (B <= 0 || H <= 0 || N_q <= 0 || N_kv <= 0 || d <= 0)
     return fail(FA_ERR_INVALID_ARG, "fa_forward: sizes must be positive (B=%d H=%d N_q=%d N_kv=%d d=%d)", B, H,
@@ -147,6 +152,8 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
     return fail(FA_ERR_INVALID_ARG, "fa_forward: q, k, v, o must be 16-byte aligned");
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
     return fail(FA_ERR_INVALID_ARG, "fa_forward: lse must be 4-byte aligned");
+  if (causal && N_q > N_kv)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward: causal attention needs N_q <= N_kv (got %d > %d)", N_q, N_kv);
   const int esz = dtype == FA_BF16 ? 2 : 4;
   int64_t st[12];
   if (strides == nullptr) {
@@ -182,6 +189,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
     p.o_sh = st[10];
     p.o_sn = st[11];
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal;
     cudaError_t e = fa::launch_fwd_bf16(d, p, s);
     if (e != cudaSuccess) return cuda_fail(e, "fa_forward launch");
     return check_launch("fa_forward", 1);
@@ -201,9 +209,28 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   p.v_sb = st[6]; p.v_sh = st[7]; p.v_sn = st[8];
   p.o_sb = st[9]; p.o_sh = st[10]; p.o_sn = st[11];
   p.scale = scale;
+  p.causal = causal;
   cudaError_t e = fa::launch_fwd_f32(d, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_forward (fp32) launch");
   return check_launch("fa_forward", 1);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                     int N_kv, int d, fa_dtype dtype, float scale, const int64_t* strides, void* stream) {
+  return forward_impl(q, k, v, o, lse, B, H, N_q, N_kv, d, dtype, scale, strides, 0, stream);
+}
+
+fa_status fa_forward_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                            int N_kv, int d, fa_dtype dtype, float scale, const int64_t* strides, fa_mask mask,
+                            void* stream) {
+  if (mask != FA_MASK_NONE && mask != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_masked: unknown mask %d", static_cast<int>(mask));
+  return forward_impl(q, k, v, o, lse, B, H, N_q, N_kv, d, dtype, scale, strides, mask == FA_MASK_CAUSAL ? 1 : 0,
+                      stream);
 }
 
 size_t fa_decode_workspace_size(int B, int H, int d, int n_splits) {
@@ -308,9 +335,13 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   return round256(rows * d * 4) + 2 * round256(rows * 4);
 }
 
-fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_dtype dtype,
-                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status backward_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_dtype dtype,
+                        float scale, void* workspace, size_t workspace_bytes, int causal, void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
     return fail(FA_ERR_INVALID_ARG, "fa_backward: null pointer");
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return fail(FA_ERR_INVALID_ARG, "fa_backward: sizes must be positive");
@@ -351,10 +382,32 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   p.N = N;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal;
   int launches = 0;
   cudaError_t e = fa::launch_bwd_bf16(d, p, static_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return cuda_fail(e, "fa_backward launch");
   return check_launch("fa_backward", launches);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_dtype dtype,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, dtype, scale, workspace, workspace_bytes, 0,
+                       stream);
+}
+
+fa_status fa_backward_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                             fa_dtype dtype, float scale, void* workspace, size_t workspace_bytes, fa_mask mask,
+                             void* stream) {
+  if (mask != FA_MASK_NONE && mask != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "fa_backward_masked: unknown mask %d", static_cast<int>(mask));
+  return backward_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, dtype, scale, workspace, workspace_bytes,
+                       mask == FA_MASK_CAUSAL ? 1 : 0, stream);
 }
 
 fa_status fa_device_status(void* stream) {

@@ -25,6 +25,10 @@
 // warp then adds 32 consecutive head-dim values of one query row, one full
 // 128-byte line per reduction instruction.
 //
+// Causal mask (query i sees key j when j <= i): key tile j only meets query
+// tiles i >= j, so the loop starts at its diagonal tile, where Pᵀ entries with
+// key > query are zeroed (and with them dSᵀ).
+//
 // Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner + MMA issuer;
 // warps 2..5 compute Pᵀ and dSᵀ (thread = key row) and write dK/dV at the end;
 // warps 6..9 drain dQ_iᵀ from TMEM (thread = head-dim index) into the accumulator.
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   const int b = blockIdx.z;
   const int64_t bh = static_cast<int64_t>(b) * p.H + h;
   const int T = p.N / kTile;
+  const int i0 = p.causal ? j : 0;  // first query tile this key tile meets
+  const int nT = T - i0;            // query tiles visited; "it" counts them from 0
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -185,9 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         tma_load_4d(smem + kOffV + kb * kTileBytes, &p.tm_v, &bars->kv_full, kb * 64, j * kTile, h, b);
       }
       int issued = 0;
-      for (int i = 0; i < T; ++i) {
-        const int qb = i & 1;
-        if (!mbar_wait(&bars->q_empty[qb], ((i >> 1) & 1) ^ 1, abort_flag, p.err, site(1))) break;
+      for (int it = 0; it < nT; ++it) {
+        const int i = i0 + it;
+        const int qb = it & 1;
+        if (!mbar_wait(&bars->q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.err, site(1))) break;
         mbar_arrive_expect_tx(&bars->q_full[qb], 2 * kOpBytes);
         for (int kb = 0; kb < 2; ++kb) {
           tma_load_4d(smem + kOffQ + qb * kOpBytes + kb * kTileBytes, &p.tm_q, &bars->q_full[qb], kb * 64,
@@ -212,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sQ = smem_u32(smem + kOffQ), sDO = smem_u32(smem + kOffDO);
       const uint32_t sDST = smem_u32(smem + kOffDST);
-      auto issue_st = [&](int i) {  // Sᵀ = K_j Q_iᵀ
-        const uint32_t q = sQ + (i & 1) * kOpBytes;
+      auto issue_st = [&](int it) {  // Sᵀ = K_j Q_iᵀ for the it-th visited query tile
+        const uint32_t q = sQ + (it & 1) * kOpBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
@@ -228,10 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         tc_fence_after();
         issue_st(0);
       }
-      for (int i = 0; ok && i < T; ++i) {
-        const uint32_t ph = i & 1;
-        const uint32_t dob = sDO + (i & 1) * kOpBytes;
-        const uint32_t qb = sQ + (i & 1) * kOpBytes;
+      for (int it = 0; ok && it < nT; ++it) {
+        const uint32_t ph = it & 1;
+        const uint32_t dob = sDO + (it & 1) * kOpBytes;
+        const uint32_t qb = sQ + (it & 1) * kOpBytes;
         // dPᵀ_i = V_j dO_iᵀ into columns that held dQ_{i−1}: wait until it is drained.
         if (!(ok = mbar_wait(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(4)))) break;
         tc_fence_after();
@@ -248,19 +255,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_bf16_ts(tmem + kColDV, tmem + kColS + kk * 8, sdesc_sw128(dob + kk * 2048, kTileBytes, 1024), kIdescKM,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+                      (it > 0 || kk > 0) ? 1u : 0u);
         // Sᵀ_{i+1} overwrites Pᵀ_i, which the dV MMAs above read first (in order).
-        if (i + 1 < T) {
-          if (!(ok = mbar_wait(&bars->q_full[(i + 1) & 1], ((i + 1) >> 1) & 1, abort_flag, p.err, site(6)))) break;
+        if (it + 1 < nT) {
+          if (!(ok = mbar_wait(&bars->q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort_flag, p.err, site(6)))) break;
           tc_fence_after();
-          issue_st(i + 1);
+          issue_st(it + 1);
         }
         if (!(ok = mbar_wait(&bars->ds_ready, ph, abort_flag, p.err, site(7)))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {  // dK += dSᵀ Q_i
           mma_bf16_ss(tmem + kColDK, sdesc_sw128(sDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
-                      sdesc_sw128(qb + kk * 2048, kTileBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+                      sdesc_sw128(qb + kk * 2048, kTileBytes, 1024), kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {  // dQ_iᵀ = K_jᵀ dSᵀ (A = K_j and B = dSᵀ, both MN-major)
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         }
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free);
-        mma_commit(&bars->q_empty[i & 1]);
+        mma_commit(&bars->q_empty[it & 1]);
       }
       mma_commit(&bars->acc_done);
       if (*abort_flag) {
@@ -289,8 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // warps; after an abort a warp keeps iterating without doing work, so no
     // warp is ever left waiting at a barrier another warp has abandoned.
     bool ok = true;
-    for (int i = 0; i < T; ++i) {
-      const uint32_t ph = i & 1;
+    for (int it = 0; it < nT; ++it) {
+      const int i = i0 + it;
+      const uint32_t ph = it & 1;
+      const bool diag = p.causal && i == j;  // mask query columns c < r (key r > query c)
       named_sync(1, 128);  // every thread is done reading the previous tile's stats
       s_lse[tr] = p.lse_log2[bh * p.N + i * kTile + tr];
       s_del[tr] = p.delta[bh * p.N + i * kTile + tr];
@@ -313,11 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = half * 64 + 2 * e;
-          pk[half * 32 + e] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(ra[2 * e]), sl2, -s_lse[c])),
-                                          ex2_approx(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -s_lse[c + 1])));
-          pk[half * 32 + 16 + e] =
-              pack_bf16x2(ex2_approx(fmaf(__uint_as_float(rb[2 * e]), sl2, -s_lse[c + 32])),
-                          ex2_approx(fmaf(__uint_as_float(rb[2 * e + 1]), sl2, -s_lse[c + 33])));
+          float a0 = ex2_approx(fmaf(__uint_as_float(ra[2 * e]), sl2, -s_lse[c]));
+          float a1 = ex2_approx(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -s_lse[c + 1]));
+          float b0 = ex2_approx(fmaf(__uint_as_float(rb[2 * e]), sl2, -s_lse[c + 32]));
+          float b1 = ex2_approx(fmaf(__uint_as_float(rb[2 * e + 1]), sl2, -s_lse[c + 33]));
+          if (diag) {
+            a0 = c < r ? 0.f : a0;
+            a1 = c + 1 < r ? 0.f : a1;
+            b0 = c + 32 < r ? 0.f : b0;
+            b1 = c + 33 < r ? 0.f : b1;
+          }
+          pk[half * 32 + e] = pack_bf16x2(a0, a1);
+          pk[half * 32 + 16 + e] = pack_bf16x2(b0, b1);
         }
       }
       {
@@ -394,8 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     const int wq = warp & 3;
     const int dcol = wq * 32 + lane;  // head-dim index (TMEM lane)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    for (int i = 0; i < T; ++i) {
-      const bool ok = mbar_wait(&bars->dq_full, i & 1, abort_flag, p.err, site(12));
+    for (int it = 0; it < nT; ++it) {
+      const int i = i0 + it;
+      const bool ok = mbar_wait(&bars->dq_full, it & 1, abort_flag, p.err, site(12));
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];

@@ -27,6 +27,11 @@
 // Shared memory holds every operand in the 128-byte-swizzled layout TMA writes:
 // blocks of [128 rows][64 bf16]; P̃_i is written there by its softmax warps.
 //
+// Causal mask (the lesson's §5 lab uses is_causal=True), bottom-right aligned:
+// row i sees keys j <= i + (N_kv − N_q).  A CTA streams only the key tiles its
+// last row can see; rows mask the rest of their diagonal tile with −∞, and
+// the heaviest query blocks are scheduled first.
+//
 // Lazy rescaling: a row keeps its reference max m until a tile's max exceeds
 // it by more than kRescaleLog2 (base-2 units).  Until then P̃ = 2^(σ'S − m) is
 // at most 2^kRescaleLog2 and O, ℓ keep accumulating against the same m, so the
@@ -91,10 +96,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * (kQT * kBM);
+  const int mt = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int m0 = mt * (kQT * kBM);
   const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int T = (p.Nkv + kBN - 1) / kBN;
+  const int off = p.Nkv - p.Nq;  // >= 0 whenever causal
+  const int kv_end = p.causal ? min(p.Nkv, m0 + kQT * kBM + off) : p.Nkv;
+  const int T = (kv_end + kBN - 1) / kBN;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -254,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         s[64 + c] = __uint_as_float(r2[c]);
         s[96 + c] = __uint_as_float(r3[c]);
       }
-      const int kv_valid = p.Nkv - j * kBN;
+      int kv_valid = p.Nkv - j * kBN;
+      if (p.causal) kv_valid = min(kv_valid, m0 + qt * kBM + row + off + 1 - j * kBN);
       if (kv_valid < kBN) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)

@@ -7,6 +7,7 @@
 // written once at the end.  Everything is fp32 with correctly rounded expf,
 // so it meets a 1e-5 bound where the tf32 tensor path (10-bit mantissa) cannot.
 //
+// With the causal mask (bottom-right aligned) row i sees keys j <= i + N_kv − N_q.
 // CTA = 16 query rows of one (b, h), 4 warps × 4 rows.  Key/value tiles of 32
 // keys are staged in shared memory; lane = key for the scores, lane = head-dim
 // slice for the P·V accumulation.
@@ -65,13 +66,14 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const FwdF32Params p)
       float dot = 0.f;
 #pragma unroll 8
       for (int t = 0; t < D; ++t) dot = fmaf(sQ[r][t], sK[lane][t], dot);
-      const float s = key_ok ? dot * p.scale : -INFINITY;
+      const bool vis = key_ok && (!p.causal || j0 + lane <= r0 + r + (p.Nkv - p.Nq));
+      const float s = vis ? dot * p.scale : -INFINITY;
       float mx = s;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float m_new = fmaxf(m[rr], mx);
       const float corr = (m[rr] == -INFINITY) ? 0.f : expf(m[rr] - m_new);
-      const float pk = key_ok ? expf(s - m_new) : 0.f;
+      const float pk = vis ? expf(s - m_new) : 0.f;
       float ps = pk;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);

@@ -24,6 +24,7 @@ struct FwdParams {
   int B, H, Nq, Nkv;
   int64_t o_sb, o_sh, o_sn;  // element strides of O
   float scale_log2;          // σ·log2(e)
+  int causal;                // query i sees keys j <= i + (Nkv − Nq); needs Nq <= Nkv
   unsigned int* err;
 };
 
@@ -36,6 +37,7 @@ struct FwdF32Params {
   int B, H, Nq, Nkv;
   int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn, v_sb, v_sh, v_sn, o_sb, o_sh, o_sn;
   float scale;
+  int causal;
 };
 
 struct DecodeParams {
@@ -69,6 +71,7 @@ struct BwdParams {
   int B, H, N;
   float scale;        // σ
   float scale_log2;   // σ·log2(e)
+  int causal;         // key j visible to query i when j <= i
   unsigned int* err;
 };
 

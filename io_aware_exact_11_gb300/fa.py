@@ -18,15 +18,18 @@ LIB_PATH = os.path.join(HERE, "libfa.so")
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(5)
 FA_BF16, FA_FP32 = 0, 1
+FA_MASK_NONE, FA_MASK_CAUSAL = 0, 1
 
 EXPORTED = (
     "fa_abi_version",
     "fa_forward",
+    "fa_forward_masked",
     "fa_decode_workspace_size",
     "fa_decode_splitkv",
     "fa_decode_splitkv_noalloc",
     "fa_backward_workspace_size",
     "fa_backward",
+    "fa_backward_masked",
     "fa_device_status",
     "fa_status_string",
     "fa_get_last_error",
@@ -55,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.fa_abi_version.restype = i32
         L.fa_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp]
         L.fa_forward.restype = i32
+        L.fa_forward_masked.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp]
+        L.fa_forward_masked.restype = i32
         L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fa_decode_workspace_size.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
@@ -63,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.fa_backward_workspace_size.restype = sz
         L.fa_backward.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, vp, sz, vp]
         L.fa_backward.restype = i32
+        L.fa_backward_masked.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, vp, sz, i32, vp]
+        L.fa_backward_masked.restype = i32
         L.fa_device_status.argtypes = [vp]
         L.fa_device_status.restype = i32
         L.fa_status_string.argtypes = [i32]
@@ -119,11 +126,13 @@ def device_status(stream=None) -> None:
     _check(lib().fa_device_status(_stream_ptr(stream)))
 
 
-def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True, stream=None):
+def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True, stream=None,
+            causal: bool = False):
     """Exact attention forward.  q [B,H,Nq,d], k/v [B,H,Nkv,d] (bf16 or fp32).
 
     Returns (O, LSE) with O like q and LSE fp32 [B,H,Nq].  Non-contiguous
-    inputs are passed by stride (d must be the contiguous dim).
+    inputs are passed by stride (d must be the contiguous dim).  ``causal``
+    masks keys j > i + Nkv − Nq for query row i.
     """
     torch = _torch()
     _check_cuda(q, k, v)
@@ -146,8 +155,12 @@ def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse:
                 raise ValueError("the head dim must be contiguous")
         arr = (ctypes.c_int64 * 12)(*[int(t.stride(i)) for t in (q, k, v, out) for i in range(3)])
         strides = ctypes.cast(arr, ctypes.c_void_p)
-    _check(lib().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d,
-                            _dtype_code(q), float(scale), strides, _stream_ptr(stream)))
+    if causal:
+        _check(lib().fa_forward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d,
+                                       _dtype_code(q), float(scale), strides, FA_MASK_CAUSAL, _stream_ptr(stream)))
+    else:
+        _check(lib().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d,
+                                _dtype_code(q), float(scale), strides, _stream_ptr(stream)))
     return out, lse
 
 
@@ -222,8 +235,11 @@ def backward_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 
 def backward(q, k, v, o, lse, do, scale: float | None = None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
-    """Gradients (dQ, dK, dV) from the saved O and LSE; all [B,H,N,d] contiguous."""
+             workspace=None, stream=None, causal: bool = False):
+    """Gradients (dQ, dK, dV) from the saved O and LSE; all [B,H,N,d] contiguous.
+
+    ``causal`` must match the forward that produced O and LSE.
+    """
     torch = _torch()
     _check_cuda(q, k, v, o, lse, do)
     B, H, N, d = q.shape
@@ -238,7 +254,10 @@ def backward(q, k, v, o, lse, do, scale: float | None = None, dq=None, dk=None, 
     need = backward_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    _check(lib().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
-                             _ptr(dv), B, H, N, d, _dtype_code(q), float(scale), _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+            _dtype_code(q), float(scale), _ptr(workspace), workspace.numel() * workspace.element_size())
+    if causal:
+        _check(lib().fa_backward_masked(*args, FA_MASK_CAUSAL, _stream_ptr(stream)))
+    else:
+        _check(lib().fa_backward(*args, _stream_ptr(stream)))
     return dq, dk, dv

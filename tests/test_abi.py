@@ -118,3 +118,18 @@ def test_backward_rejects_bad_arguments(L):
     assert bwd(wsb=10) == fa.FA_ERR_INVALID_ARG
     assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert bwd(ws=None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_masked_entry_points_validate_before_cuda(L):
+    def fwdm(mask=fa.FA_MASK_CAUSAL, nq=128, nkv=128):
+        return L.fa_forward_masked(FAKE, FAKE, FAKE, FAKE, None, 1, 1, nq, nkv, 128, fa.FA_BF16, 0.1, None, mask,
+                                   None)
+    assert fwdm(mask=5) == fa.FA_ERR_INVALID_ARG
+    assert fwdm(nq=200, nkv=100) == fa.FA_ERR_INVALID_ARG      # causal needs N_q <= N_kv
+    assert b"causal" in L.fa_get_last_error()
+
+    def bwdm(mask=fa.FA_MASK_CAUSAL, n=200):
+        return L.fa_backward_masked(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, n, 128, fa.FA_BF16,
+                                    0.1, FAKE, 1 << 24, mask, None)
+    assert bwdm(mask=-1) == fa.FA_ERR_INVALID_ARG
+    assert bwdm(n=200) == fa.FA_ERR_UNSUPPORTED

@@ -1,0 +1,116 @@
+"""GPU parity of the causal mask (bottom-right aligned: query i of Nq sees
+keys j <= i + Nkv − Nq) against the float64 oracle, forward and backward.
+
+Tolerances as for the unmasked paths: bf16 O within 1e-2 max-abs, LSE within
+1e-3, fp32 within 1e-5, gradients within 2e-2 relative L2.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_exact_11_gb300 import fa
+from tests.gpu_helpers import cpu64, f64, make_qkv, max_abs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL_O_BF16, TOL_LSE_BF16, TOL_FP32, TOL_GRAD = 1e-2, 1e-3, 1e-5, 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.lib()
+    yield
+    fa.device_status()
+
+
+def _check(seed, B, H, Nq, Nkv, d, dtype, tol_o, tol_lse):
+    host, dev = make_qkv(seed, B, H, Nq, Nkv, d, dtype)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale, causal=True)
+    fa.device_status()
+    ro, rl = oracle.attention_forward(f64(host["q"], dtype), f64(host["k"], dtype), f64(host["v"], dtype), scale,
+                                      causal=True)
+    eo, el = max_abs(cpu64(o), ro), max_abs(cpu64(lse), rl)
+    assert eo <= tol_o and el <= tol_lse, (eo, el)
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 2, 256, 256, 128),     # two query tiles = one CTA
+    (2, 3, 300, 300, 128),     # ragged tail
+    (1, 2, 200, 457, 128),     # Nq < Nkv: rows offset by 257
+    (1, 1, 1, 129, 128),       # one query row sees every key
+    (1, 2, 640, 640, 64),      # head dim 64
+    (1, 1, 1000, 1000, 128),   # several CTAs of different lengths
+])
+def test_causal_forward_bf16(shape):
+    _check(21, *shape, "bf16", TOL_O_BF16, TOL_LSE_BF16)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 256, 256, 64), (2, 2, 77, 100, 128)])
+def test_causal_forward_fp32(shape):
+    _check(22, *shape, "fp32", TOL_FP32, TOL_FP32)
+
+
+def test_causal_rejects_more_queries_than_keys():
+    import torch
+    x = torch.zeros((1, 1, 256, 128), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FAError) as ei:
+        fa.forward(x, y, y, causal=True)
+    assert ei.value.status == fa.FA_ERR_INVALID_ARG
+
+
+def test_causal_last_query_row_equals_unmasked():
+    """With Nq = 1 the single row sees every key: causal equals unmasked."""
+    import torch
+    _, dev = make_qkv(23, 2, 3, 1, 777, 128, "bf16")
+    o1, l1 = fa.forward(dev["q"], dev["k"], dev["v"], causal=True)
+    o2, l2 = fa.forward(dev["q"], dev["k"], dev["v"])
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.slow
+def test_causal_prefill_full_size_sampled():
+    B, H, N, d = 4, 32, 4096, 128
+    host, dev = make_qkv(24, B, H, N, N, d, "bf16")
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale, causal=True)
+    fa.device_status()
+    rng = np.random.default_rng(11)
+    for n, (b, h) in enumerate([(0, 0), (3, 31), (1, 7), (2, 19)]):
+        rows = np.arange(N) if n == 0 else np.concatenate([[0, 1, 127, 128, 255, 256, N - 1],
+                                                           np.sort(rng.choice(N, 48, replace=False))])
+        ro, rl = oracle.attention_rows(f64(host["q"][b, h], "bf16"), f64(host["k"][b, h], "bf16"),
+                                       f64(host["v"][b, h], "bf16"), scale, rows, causal=True)
+        assert max_abs(cpu64(o[b, h])[rows], ro) <= TOL_O_BF16
+        assert max_abs(cpu64(lse[b, h])[rows], rl) <= TOL_LSE_BF16
+
+
+def _bwd(seed, B, H, N, heads=None):
+    d = 128
+    host, dev = make_qkv(seed, B, H, N, N, d, "bf16", with_do=True)
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale, causal=True)
+    dq, dk, dv = fa.backward(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], scale, causal=True)
+    fa.device_status()
+    for b, h in heads or [(b, h) for b in range(B) for h in range(H)]:
+        rq, rk, rv = oracle.attention_backward(*(f64(host[n][b, h], "bf16") for n in ("q", "k", "v", "do")), scale,
+                                               causal=True)
+        e = (rel_l2(cpu64(dq[b, h]), rq), rel_l2(cpu64(dk[b, h]), rk), rel_l2(cpu64(dv[b, h]), rv))
+        assert max(e) <= TOL_GRAD, ((b, h), e)
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 2, 128), (1, 2, 256), (2, 1, 640)])
+def test_causal_backward(B, H, N):
+    _bwd(25, B, H, N)
+
+
+@pytest.mark.slow
+def test_causal_backward_train_full_size_sampled():
+    _bwd(26, 2, 16, 8192, heads=[(0, 3), (1, 12)])
