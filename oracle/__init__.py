@@ -7,6 +7,7 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
 from .attention import (  # noqa: F401
     attention_backward,
     attention_forward,
+    attention_forward_gqa,
     attention_probs,
     attention_rows,
     backward_delta,

@@ -35,6 +35,10 @@ Every function computes in float64.  What each one follows:
   memory lab (§5, ``is_causal=True``), bottom-right aligned: query i of Nq
   sees keys j <= i + (Nk − Nq).  Masked scores are −∞ before the softmax,
   the plain definition with those entries removed.
+* ``attention_forward_gqa``: grouped-query attention as used by the model the
+  lesson's lab takes its shapes from (Qwen2.5-7B, [Lesson] §5): query head h
+  reads key/value head h // G, G = H_q / H_kv.  Written as that index map over
+  the plain definition.
 * ``attention_backward``: the pages give no gradient formulas, only that the
   backward recomputes S and P from Q, K, V and the saved statistics
   ([Walk] "Flash Attention Backward", [Notes] §二.5).  The oracle uses the
@@ -55,6 +59,7 @@ __all__ = [
     "attention_probs",
     "attention_forward",
     "attention_rows",
+    "attention_forward_gqa",
     "online_attention",
     "split_partials",
     "merge_partials",
@@ -187,6 +192,27 @@ def online_attention(q, k, v, scale: float, block: int):
         acc = corr[:, None] * acc + p @ v[j0:j0 + block]
         m = m_new
     return acc / l[:, None], m + np.log(l)
+
+
+def attention_forward_gqa(q, k, v, scale: float, causal: bool = False):
+    """Grouped-query attention: q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d], Hq % Hkv == 0.
+
+    Query head h attends with key/value head h // (Hq / Hkv); everything else
+    is ``attention_forward``.  Returns (O [B, Hq, Nq, d], LSE [B, Hq, Nq]).
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    B, Hq = q.shape[:2]
+    Hkv = k.shape[1]
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    o = np.empty(q.shape[:3] + (v.shape[-1],))
+    lse = np.empty(q.shape[:3])
+    for b in range(B):
+        for h in range(Hq):
+            o[b, h], lse[b, h] = attention_forward(q[b, h], k[b, h // G], v[b, h // G], scale, causal=causal)
+    return o, lse
 
 
 def split_partials(q, k, v, scale: float, n_splits: int):

@@ -340,3 +340,27 @@ def test_causal_backward_matches_finite_differences():
         assert np.linalg.norm(num - g) / np.linalg.norm(num) <= 1e-6, name
     # The last key only reaches the last query row.
     assert np.allclose(dv[-1], oracle.attention_probs(q, k, scale, True)[-1, -1] * do[-1], atol=1e-14)
+
+
+# --------------------------------------------------------- grouped queries
+
+
+def test_gqa_equals_standard_attention_on_repeated_heads():
+    """Independent route: repeat each K/V head G times and use the plain path."""
+    B, Hq, Hkv, N, d = 2, 6, 2, 9, 4
+    q = RNG.standard_normal((B, Hq, 1, d))
+    k = RNG.standard_normal((B, Hkv, N, d))
+    v = RNG.standard_normal((B, Hkv, N, d))
+    o, lse = oracle.attention_forward_gqa(q, k, v, 0.5)
+    o2, lse2 = oracle.attention_forward(q, np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1), 0.5)
+    assert np.allclose(o, o2, atol=1e-15) and np.allclose(lse, lse2, atol=1e-15)
+    # Heads of one group differ only through their queries.
+    o3, _ = oracle.attention_forward_gqa(np.repeat(q[:, :1], 6, axis=1), k, v, 0.5)
+    assert np.allclose(o3[:, 0], o3[:, 2], atol=1e-15) and not np.allclose(o3[:, 0], o3[:, 3])
+
+
+def test_gqa_with_one_group_is_standard():
+    q = RNG.standard_normal((1, 3, 4, 5))
+    k = RNG.standard_normal((1, 3, 7, 5))
+    v = RNG.standard_normal((1, 3, 7, 5))
+    assert np.allclose(oracle.attention_forward_gqa(q, k, v, 0.3)[0], oracle.attention_forward(q, k, v, 0.3)[0])
