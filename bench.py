@@ -354,6 +354,24 @@ def run_ours(args, ws, rank, local):
                                         "traffic": None if dec_traffic is None else dec_traffic * Bd / 64}}
         del qd, kd, vd, od, ld, ws_d
 
+    if "gqa" in extras:
+        # ---------------- grouped-query decode, the lab model's 28 query / 4 key-value heads
+        Bg, Hq, Hkv, Ng, S = args.decode_batch, 28, 4, DECODE["N"], DECODE["splits"]
+        qg = randn((Bg, Hq, 1, d), 21)
+        kg, vg = randn((Bg, Hkv, Ng, d), 22), randn((Bg, Hkv, Ng, d), 23)
+        og = torch.empty_like(qg)
+        lg = torch.empty((Bg, Hq), dtype=torch.float32, device=dev)
+        ws_g = torch.empty(fa.decode_workspace_size(Bg, Hq, d, S), dtype=torch.uint8, device=dev)
+        n_g = max(5, min(args.steps, 50))
+        # K/V (1.07 GB at B=64) is larger than L2, so back-to-back steps stream it from HBM.
+        t_g = timed(lambda: fa.decode_splitkv_gqa(qg, kg, vg, n_splits=S, out=og, lse=lg, workspace=ws_g),
+                    n_g, 2) / n_g
+        kvb = 2.0 * Bg * Hkv * Ng * d * 2
+        extra["gqa_decode"] = {"workload": f"B={Bg} Hq=28 Hkv=4 S_q=1 N_kv=8192 d=128 bf16, 32 splits",
+                               "hbm_gbs": kvb / t_g / 1e9, "tokens_per_s": Bg / t_g, "ms": t_g * 1e3,
+                               "frac_of_hbm_peak": kvb / t_g / 1e9 / float(peaks["hbm_gbs"])}
+        del qg, kg, vg, og, lg, ws_g
+
     if "train" in extras:
         # ---------------- training forward + backward
         Bt, Ht, Nt = TRAIN["B"], TRAIN["H"], TRAIN["N"]
@@ -441,7 +459,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
-    ap.add_argument("--extras", default="long,decode,train,causal",
+    ap.add_argument("--extras", default="long,decode,gqa,train,causal",
                     help="comma list of extra workloads measured after the headline")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="decode batch B (64 is the configured workload; smaller only for profiling)")

@@ -123,6 +123,21 @@ FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, 
                             int n_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_decode_splitkv_gqa — fa_decode_splitkv with grouped query heads.
+ *   H_q query heads share H_kv key/value heads: query head h reads key/value
+ *   head h / (H_q / H_kv), the grouped-query layout of the model whose shapes
+ *   the lesson's lab uses (Qwen2.5-7B: 28 query heads, 4 key/value heads).  One
+ *   CTA per (b, key/value head, chunk) reads each K/V byte once for the whole
+ *   group, so the decode stays bound by the K/V bytes of H_kv heads.
+ *   q [B,H_q,1,d], k and v [B,H_kv,N_kv,d] contiguous; o [B,H_q,1,d]; lse [B,H_q]
+ *   (or NULL).  workspace: fa_decode_workspace_size(B, H_q, d, n_splits) bytes.
+ *   Supported: FA_BF16, d = 128, H_q = G·H_kv with 1 <= G <= 8, 1 ≤ n_splits ≤ 256.
+ */
+FA_API fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                                       int B, int H_q, int H_kv, int N_kv, int d, fa_dtype dtype, float scale,
+                                       int n_splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fa_decode_splitkv_noalloc — fa_decode_splitkv for callers that cannot pass a
  * workspace.  The pages have no counterpart: this is a deployment variant.
  *   Who it is for: callers that cannot allocate device memory when they decode,

@@ -329,6 +329,54 @@ fa_status fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v,
   return check_launch("fa_decode_splitkv_noalloc", 2);
 }
 
+fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                                int H_kv, int N_kv, int d, fa_dtype dtype, float scale, int n_splits, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !workspace) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: null pointer");
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || N_kv <= 0 || d <= 0 || n_splits <= 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: sizes must be positive");
+  if (H_q % H_kv != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: unknown dtype");
+  if (dtype != FA_BF16 || d != 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: only bf16 with d=128 is built");
+  if (H_q / H_kv > 8)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: at most 8 query heads per key/value head (got %d)",
+                H_q / H_kv);
+  if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: n_splits must be <= 256");
+  if (B > 65535 || H_q > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: B and H must be <= 65535");
+  if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: scale must be finite and > 0");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: pointers must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: lse must be 4-byte aligned");
+  const size_t need = fa_decode_workspace_size(B, H_q, d, n_splits);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: workspace %zu bytes, need %zu", workspace_bytes, need);
+  fa::DecodeParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  const size_t slots = static_cast<size_t>(B) * H_q * n_splits;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(slots * d * 4));
+  p.B = B;
+  p.H = H_q;
+  p.Hkv = H_kv;
+  p.G = H_q / H_kv;
+  p.Nkv = N_kv;
+  p.n_splits = n_splits;
+  p.chunk = (N_kv + n_splits - 1) / n_splits;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  fa_status r = watchdog_ptr(&p.err);
+  if (r != FA_OK) return r;
+  cudaError_t e = fa::launch_decode_bf16(d, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_gqa launch");
+  return check_launch("fa_decode_splitkv_gqa", 2);
+}
+
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N;

@@ -41,8 +41,8 @@ struct FwdF32Params {
 };
 
 struct DecodeParams {
-  const void* q;  // [B,H,d] bf16
-  const void* k;  // [B,H,N,d] bf16
+  const void* q;  // [B,H,d] bf16 (H query heads)
+  const void* k;  // [B,Hkv,N,d] bf16
   const void* v;
   void* o;        // [B,H,d] bf16
   float* lse;     // [B,H] or null
@@ -51,6 +51,8 @@ struct DecodeParams {
   int B, H, Nkv, n_splits, chunk;
   float scale_log2;
   unsigned int* err;
+  int Hkv = 0;    // key/value heads; 0 means H (one query head per key/value head)
+  int G = 1;      // query heads per key/value head, H = Hkv·G
 };
 
 struct BwdParams {

@@ -26,6 +26,7 @@ EXPORTED = (
     "fa_forward_masked",
     "fa_decode_workspace_size",
     "fa_decode_splitkv",
+    "fa_decode_splitkv_gqa",
     "fa_decode_splitkv_noalloc",
     "fa_backward_workspace_size",
     "fa_backward",
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.fa_decode_workspace_size.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
         L.fa_decode_splitkv.restype = i32
+        L.fa_decode_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+        L.fa_decode_splitkv_gqa.restype = i32
         L.fa_backward_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fa_backward_workspace_size.restype = sz
         L.fa_backward.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, vp, sz, vp]
@@ -192,6 +195,33 @@ def decode_splitkv(q, k, v, n_splits: int = 32, scale: float | None = None, out=
     _check(lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nkv, d,
                                    _dtype_code(q), float(scale), int(n_splits), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+def decode_splitkv_gqa(q, k, v, n_splits: int = 32, scale: float | None = None, out=None, lse=None,
+                       workspace=None, stream=None):
+    """Grouped-query split-KV decode: q [B,Hq,1,d], k/v [B,Hkv,Nkv,d], Hq = G·Hkv (G <= 8)."""
+    torch = _torch()
+    _check_cuda(q, k, v)
+    B, Hq, one, d = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if one != 1:
+        raise ValueError("decode takes one query row per head")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("decode inputs must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, 1, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(B, Hq, d, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().fa_decode_splitkv_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nkv, d,
+                                       _dtype_code(q), float(scale), int(n_splits), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return out, lse
 
 
