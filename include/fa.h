@@ -128,7 +128,9 @@ FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, 
  *   head h / (H_q / H_kv), the grouped-query layout of the model whose shapes
  *   the lesson's lab uses (Qwen2.5-7B: 28 query heads, 4 key/value heads).  One
  *   CTA per (b, key/value head, chunk) reads each K/V byte once for the whole
- *   group, so the decode stays bound by the K/V bytes of H_kv heads.
+ *   group: with G = 1 this is fa_decode_splitkv; with G >= 2 the group's query
+ *   rows go through tcgen05 MMAs (S = Q_g K_jᵀ, O += P̃ V_j), because 2·G·d
+ *   multiply-adds per key would outrun CUDA cores long before the HBM stream.
  *   q [B,H_q,1,d], k and v [B,H_kv,N_kv,d] contiguous; o [B,H_q,1,d]; lse [B,H_q]
  *   (or NULL).  workspace: fa_decode_workspace_size(B, H_q, d, n_splits) bytes.
  *   Supported: FA_BF16, d = 128, H_q = G·H_kv with 1 <= G <= 8, 1 ≤ n_splits ≤ 256.

@@ -372,8 +372,35 @@ fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, voi
   p.scale_log2 = scale * 1.4426950408889634f;
   fa_status r = watchdog_ptr(&p.err);
   if (r != FA_OK) return r;
-  cudaError_t e = fa::launch_decode_bf16(d, p, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.G == 1) {
+    cudaError_t e = fa::launch_decode_bf16(d, p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_gqa launch");
+    return check_launch("fa_decode_splitkv_gqa", 2);
+  }
+  // Groups of two or more query heads: tensor-core split kernel, then the merge.
+  fa::DecodeTcParams t;
+  memset(&t, 0, sizeof(t));
+  const int64_t qspan = static_cast<int64_t>(B) * H_q * d;  // q as one [B·H_q, d] matrix
+  if ((r = make_map(&t.tm_q, q, 1, 1, B * H_q, d, qspan, qspan, d, "q")) != FA_OK) return r;
+  const int64_t nd = static_cast<int64_t>(N_kv) * d;
+  if ((r = make_map(&t.tm_k, k, B, H_kv, N_kv, d, H_kv * nd, nd, d, "k")) != FA_OK) return r;
+  if ((r = make_map(&t.tm_v, v, B, H_kv, N_kv, d, H_kv * nd, nd, d, "v")) != FA_OK) return r;
+  t.part_o = p.part_o;
+  t.part_ml = p.part_ml;
+  t.B = B;
+  t.Hq = H_q;
+  t.Hkv = H_kv;
+  t.G = p.G;
+  t.Nkv = N_kv;
+  t.n_splits = n_splits;
+  t.chunk = p.chunk;
+  t.scale_log2 = p.scale_log2;
+  t.err = p.err;
+  cudaError_t e = fa::launch_decode_gqa_tc(t, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_gqa launch");
+  e = fa::launch_decode_merge(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_gqa merge launch");
   return check_launch("fa_decode_splitkv_gqa", 2);
 }
 

@@ -5,9 +5,8 @@
 // §3.3 and §9: the single query's scores are a 1×N vector; FlashDecoding
 // splits the key range across SMs to keep them all busy).
 //
-// Kernel 1 (grid = splits × H_kv × B, 128 threads): CTA c streams keys
-// [c·chunk, (c+1)·chunk) of one (b, key/value head) in sub-chunks of 64 keys,
-// for the one query head (or the group of query heads) that reads it.  K and V rows
+// Kernel 1 (grid = splits × H × B, 128 threads): CTA c streams keys
+// [c·chunk, (c+1)·chunk) of one (b, h) in sub-chunks of 64 keys.  K and V rows
 // of a sub-chunk are contiguous in memory, so each arrives with one untiled bulk
 // copy per tensor into a 2-stage shared-memory ring.  The CTA runs the online
 // softmax over its keys and writes the unnormalised triple (m_c, ℓ_c, o_c).
@@ -29,10 +28,9 @@ constexpr int kStageBytes = 2 * kSub * kRowBytes;  // K then V: 32 KB
 constexpr int kThreads = 128;
 constexpr int kSmem = 2 * kStageBytes + 1024;
 
-template <int GM>
 struct DecodeSmem {
-  float scores[GM][kSub];
-  float probs[GM][kSub];
+  float scores[kSub];
+  float probs[kSub];
   float red[8][kD];
   uint64_t full[2];
   int abort_flag;
@@ -49,35 +47,27 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
-// One CTA per (split c, key/value head, b).  GM is the largest group size the
-// instantiation handles: GM = 1 is the one-query-head-per-KV-head path; for
-// grouped queries (GM = 8) the CTA serves the p.G ≤ 8 query heads that share
-// its key/value head, so every K/V byte is read once for the whole group.
-template <int GM>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
   uint8_t* ring = smem_raw + pad;
-  __shared__ DecodeSmem<GM> sm;
+  __shared__ DecodeSmem sm;
 
   const int c = blockIdx.x;
-  const int hkv = blockIdx.y;
+  const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int Hkv = gridDim.y;
-  const int G = GM == 1 ? 1 : p.G;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int dchunk = lane & 15;   // 8 head-dim values per lane
   const int kpar = lane >> 4;     // which of the two keys a warp handles at once
-  const int64_t bkv = static_cast<int64_t>(b) * Hkv + hkv;
-  const int64_t bq0 = static_cast<int64_t>(b) * p.H + static_cast<int64_t>(hkv) * G;  // first query head
+  const int64_t bh = static_cast<int64_t>(b) * p.H + h;
   const int key0 = c * p.chunk;
   const int nkeys = max(0, min(p.Nkv, key0 + p.chunk) - key0);
   const int nsub = (nkeys + kSub - 1) / kSub;
 
-  const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k) + (bkv * p.Nkv + key0) * kRowBytes;
-  const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v) + (bkv * p.Nkv + key0) * kRowBytes;
+  const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k) + (bh * p.Nkv + key0) * kRowBytes;
+  const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v) + (bh * p.Nkv + key0) * kRowBytes;
 
   if (tid == 0) {
     mbar_init(&sm.full[0], 1);
@@ -100,28 +90,18 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     if (nsub > 1) issue(1);
   }
 
-  // This lane's slice of each query head (8 values), widened to fp32.
-  float qf[GM][8];
-#pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    if (g < G) {
-      const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.q) + (bq0 + g) * kRowBytes +
-                                                      dchunk * 16);
-      bf16x8_to_f32(u, qf[g]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[g][e] = 0.f;
-    }
+  // This lane's slice of q (8 values), widened to fp32.
+  float qf[8];
+  {
+    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.q) + bh * kRowBytes +
+                                                    dchunk * 16);
+    bf16x8_to_f32(u, qf);
   }
   const float sl2 = p.scale_log2;
-  float m_run[GM], l_run[GM], acc[GM][8];
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[8];
 #pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    m_run[g] = -INFINITY;
-    l_run[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-  }
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 
   int issued = min(nsub, 2);
   bool ok = true;
@@ -139,68 +119,48 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
       const int key = warp * 16 + pr * 2 + kpar;
       float kf[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + key * kRowBytes + dchunk * 16), kf);
+      float dot = 0.f;
 #pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        if (g < G) {
-          float dot = 0.f;
+      for (int e = 0; e < 8; ++e) dot = fmaf(qf[e], kf[e], dot);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dot = fmaf(qf[g][e], kf[e], dot);
-#pragma unroll
-          for (int o = 8; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-          if (dchunk == 0) sm.scores[g][key] = (key < n) ? dot * sl2 : -INFINITY;
-        }
-      }
+      for (int o = 8; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (dchunk == 0) sm.scores[key] = (key < n) ? dot * sl2 : -INFINITY;
     }
     __syncthreads();
 
-    // Online softmax over this sub-chunk, per query head (every warp computes
-    // the same values, so each thread holds the rescale factors it needs).
-    float corr[GM];
+    // Online softmax over this sub-chunk (every warp computes the same values).
+    const float s0 = sm.scores[lane];
+    const float s1 = sm.scores[lane + 32];
+    float mx = fmaxf(s0, s1);
 #pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      corr[g] = 1.f;
-      if (g < G) {
-        const float s0 = sm.scores[g][lane];
-        const float s1 = sm.scores[g][lane + 32];
-        float mx = fmaxf(s0, s1);
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float m_new = fmaxf(m_run, mx);
+    const float corr = ex2_approx(m_run - m_new);
+    const float p0 = ex2_approx(s0 - m_new);
+    const float p1 = ex2_approx(s1 - m_new);
+    float ps = p0 + p1;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float m_new = fmaxf(m_run[g], mx);
-        corr[g] = ex2_approx(m_run[g] - m_new);
-        const float p0 = ex2_approx(s0 - m_new);
-        const float p1 = ex2_approx(s1 - m_new);
-        float ps = p0 + p1;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        l_run[g] = l_run[g] * corr[g] + ps;
-        m_run[g] = m_new;
-        if (warp == 0) {
-          sm.probs[g][lane] = p0;
-          sm.probs[g][lane + 32] = p1;
-        }
-      }
+    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    l_run = l_run * corr + ps;
+    m_run = m_new;
+    if (warp == 0) {
+      sm.probs[lane] = p0;
+      sm.probs[lane + 32] = p1;
     }
     __syncthreads();
 
     // P·V: lane owns 8 head-dim values; the 8 (warp, half) groups split the keys.
 #pragma unroll
-    for (int g = 0; g < GM; ++g)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] *= corr[g];
+    for (int e = 0; e < 8; ++e) acc[e] *= corr;
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) {
       const int key = ii * 8 + warp * 2 + kpar;
       if (key < n) {
+        const float pk = sm.probs[key];
         float vf[8];
         bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + key * kRowBytes + dchunk * 16), vf);
 #pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          if (g < G) {
-            const float pk = sm.probs[g][key];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pk, vf[e], acc[g][e]);
-          }
-        }
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pk, vf[e], acc[e]);
       }
     }
     __syncthreads();
@@ -216,25 +176,19 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     return;
   }
 
-  // Per query head: combine the 8 key groups, then write the unnormalised triple.
-  const int grp = warp * 2 + kpar;
+  // Combine the 8 key groups, then write the unnormalised triple.
+  const int g = warp * 2 + kpar;
 #pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    if (g < G) {
-      if (g > 0) __syncthreads();  // the previous head's sums have been read
+  for (int e = 0; e < 8; ++e) sm.red[g][dchunk * 8 + e] = acc[e];
+  __syncthreads();
+  float o = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sm.red[grp][dchunk * 8 + e] = acc[g][e];
-      __syncthreads();
-      float o = 0.f;
-#pragma unroll
-      for (int gg = 0; gg < 8; ++gg) o += sm.red[gg][tid];
-      const int64_t slot = (bq0 + g) * p.n_splits + c;
-      p.part_o[slot * kD + tid] = o;
-      if (tid == 0) {
-        p.part_ml[slot * 2 + 0] = m_run[g];  // −∞ and ℓ = 0 for a split with no keys
-        p.part_ml[slot * 2 + 1] = l_run[g];
-      }
-    }
+  for (int gg = 0; gg < 8; ++gg) o += sm.red[gg][tid];
+  const int64_t slot = bh * p.n_splits + c;
+  p.part_o[slot * kD + tid] = o;
+  if (tid == 0) {
+    p.part_ml[slot * 2 + 0] = m_run;  // −∞ and ℓ = 0 for a split with no keys
+    p.part_ml[slot * 2 + 1] = l_run;
   }
 }
 
@@ -258,20 +212,16 @@ __global__ void __launch_bounds__(kD) decode_merge_kernel(const DecodeParams p) 
 
 }  // namespace
 
+cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
+  decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t stream) {
-  if (d != kD) return cudaErrorInvalidValue;
-  const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
-  if (p.G < 1 || p.G > 8 || hkv * p.G != p.H) return cudaErrorInvalidValue;
-  cudaError_t e;
-  if (p.G == 1) {
-    e = cudaFuncSetAttribute(decode_split_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    decode_split_kernel<1><<<dim3(p.n_splits, hkv, p.B), kThreads, kSmem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(decode_split_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    decode_split_kernel<8><<<dim3(p.n_splits, hkv, p.B), kThreads, kSmem, stream>>>(p);
-  }
+  if (d != kD || p.G != 1) return cudaErrorInvalidValue;  // groups go to the tensor-core kernel
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);

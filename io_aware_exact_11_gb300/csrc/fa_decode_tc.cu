@@ -1,0 +1,330 @@
+// fa_decode_tc.cu — grouped-query split-KV decode on tcgen05 tensor cores.
+//
+// With G query heads per key/value head, each key costs 2·G·d multiply-adds
+// per byte pair of K and V read, which at G ≥ 2 outgrows what CUDA cores hide
+// under the HBM stream.  Here the G query rows of one (b, key/value head) form
+// the first rows of a 128-row A tile (the rest are neighbouring rows that never
+// leave the CTA), and each key tile goes through the tensor cores:
+//   S = Q_g K_jᵀ (tcgen05.mma → TMEM), online softmax of §3.2 of
+//   "FlashAttention：IO-aware 的注意力 kernel" on rows 0..G−1, O += P̃ V_j.
+// The CTA covers one chunk of the key range (FlashDecoding's split, §3.3 and
+// §9 of the same lesson) and writes unnormalised (m, ℓ, o) triples that the
+// split-KV merge kernel folds with the block-merge rule (omica.com.cn news
+// 1422242, §二.3).
+//
+// Warp roles (96 threads): warp 0 softmax for TMEM lanes 0..31 (rows 0..31 of
+// the A tile; rows ≥ G are padding) and the epilogue; warp 1 TMA producer
+// (Q once, then K_0, K_1, V_0, K_2, V_1, … into a 3-slot ring); warp 2 TMEM
+// owner and MMA issuer.  TMEM: S buffers at columns 0 and 128, O at 256.
+// Rows keep their reference max until a tile's max exceeds it by 2^8 (base 2),
+// exactly as in the forward kernel; the merge accepts any reference m.
+#include "fa_kernels.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBN = 128;
+constexpr int kTileBytes = 128 * 128;    // [128 rows][64 bf16], 128-byte swizzle
+constexpr int kSlot = 2 * kTileBytes;    // one 128 × 128 bf16 tile
+constexpr int kRing = 3;
+constexpr int kThreads = 96;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.0f;
+
+constexpr int kOffQ = 0;
+constexpr int kOffR = kOffQ + kSlot;
+constexpr int kOffP = kOffR + kRing * kSlot;
+constexpr int kOffBar = kOffP + kSlot;
+constexpr int kSmem = kOffBar + 256 + 1024;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t r_full[kRing], r_empty[kRing];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, p_free;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+__device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernDecode << 8) | (0x80u | s); }
+__device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int seq_v(int j, int T) { return min(2 * j + 2, 2 * T - 1); }
+
+__global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid_constant__ DecodeTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const int hkv = blockIdx.y;
+  const int b = blockIdx.z;
+  const int qrow0 = b * p.Hq + hkv * p.G;  // first query row in the [B·H_q, d] view
+  const int key0 = c * p.chunk;
+  const int kend = min(p.Nkv, key0 + p.chunk);
+  const int nkeys = max(0, kend - key0);
+  const int T = (nkeys + kBN - 1) / kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&bars->r_full[s], 1);
+      mbar_init(&bars->r_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 32);
+    }
+    mbar_init(&bars->p_full, 32);
+    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && T > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(&bars->q_full, kSlot);
+      for (int kb = 0; kb < 2; ++kb)
+        tma_load_4d(smem + kOffQ + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64, qrow0, 0, 0);
+      int issued = 0;
+      for (int t = 0; t < 2 * T; ++t) {
+        const int slot = t % kRing;
+        const uint32_t u = t / kRing;
+        bool is_v;
+        int jt;
+        if (t == 0) { is_v = false; jt = 0; }
+        else if (t == 2 * T - 1) { is_v = true; jt = T - 1; }
+        else if (t & 1) { is_v = false; jt = (t + 1) >> 1; }
+        else { is_v = true; jt = (t - 2) >> 1; }
+        if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        mbar_arrive_expect_tx(&bars->r_full[slot], kSlot);
+        const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
+                      key0 + jt * kBN, hkv, b);
+        ++issued;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(&bars->q_full, 0, 200000000ull);
+        for (int t = (issued > kRing ? issued - kRing : 0); t < issued; ++t)
+          mbar_wait_drain(&bars->r_full[t % kRing], (t / kRing) & 1, 200000000ull);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(128, kBN, false, false);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t sQ = smem_u32(smem + kOffQ);
+      const uint32_t sR = smem_u32(smem + kOffR);
+      const uint32_t sP = smem_u32(smem + kOffP);
+      auto issue_pv = [&](int jj) -> bool {
+        const int t = seq_v(jj, T);
+        const int slot = t % kRing;
+        if (!mbar_wait(&bars->p_full, jj & 1, abort_flag, p.err, site(2))) return false;
+        if (!mbar_wait(&bars->r_full[slot], (t / kRing) & 1, abort_flag, p.err, site(3))) return false;
+        tc_fence_after();
+        const uint32_t vb = sR + slot * kSlot;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ss(tmem + kColO, sdesc_sw128(sP + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
+                      sdesc_sw128(vb + kk * 2048, kTileBytes, 1024), kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->p_free);
+        mma_commit(&bars->r_empty[slot]);
+        return true;
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, site(4));
+      for (int j = 0; ok && j < T; ++j) {
+        const int t = seq_k(j);
+        const int slot = t % kRing;
+        const int sb = j & 1;
+        ok = mbar_wait(&bars->r_full[slot], (t / kRing) & 1, abort_flag, p.err, site(5)) &&
+             mbar_wait(&bars->s_free[sb], ((j >> 1) & 1) ^ 1, abort_flag, p.err, site(6));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = sR + slot * kSlot;
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + sb * kBN, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescS,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[sb]);
+        mma_commit(&bars->r_empty[slot]);
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) issue_pv(T - 1);
+      if (*abort_flag) {
+        mma_commit(&bars->drain);
+        mbar_wait_drain(&bars->drain, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------- softmax for rows 0..31, epilogue
+    const int row = lane;  // TMEM lane; rows < G are the group's query heads
+    const float sl2 = p.scale_log2;
+    uint8_t* sP = smem + kOffP;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(&bars->s_full[sb], (j >> 1) & 1, abort_flag, p.err, site(7));
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      const uint32_t sa = tmem + sb * kBN;
+      tmem_ld32(sa + 0, r0);
+      tmem_ld32(sa + 32, r1);
+      tmem_ld32(sa + 64, r2);
+      tmem_ld32(sa + 96, r3);
+      tmem_wait_ld();
+      reg_fence(r0);
+      reg_fence(r1);
+      reg_fence(r2);
+      reg_fence(r3);
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[sb]);
+      float s[128];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        s[e] = __uint_as_float(r0[e]);
+        s[32 + e] = __uint_as_float(r1[e]);
+        s[64 + e] = __uint_as_float(r2[e]);
+        s[96 + e] = __uint_as_float(r3[e]);
+      }
+      const int valid = kend - (key0 + j * kBN);  // keys past the chunk belong to the next split
+      if (valid < kBN) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (e >= valid) s[e] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int e = 8; e < 128; e += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[e + i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_cand = fmaxf(m_run, mx * sl2);
+      const bool need = m_cand > m_run + kRescaleLog2;
+      const float m_new = need ? m_cand : m_run;
+      const float corr = need ? ex2_approx(m_run - m_new) : 1.f;
+      float rs8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 128; e += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          s[e + i] = ex2_approx(fmaf(s[e + i], sl2, -m_new));
+          rs8[i] += s[e + i];
+        }
+      l_run = l_run * corr + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+
+      ok = mbar_wait(&bars->p_free, (j & 1) ^ 1, abort_flag, p.err, site(8));
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+#pragma unroll
+      for (int c8 = 0; c8 < 16; ++c8) {
+        uint4 v;
+        v.x = pack_bf16x2(s[8 * c8 + 0], s[8 * c8 + 1]);
+        v.y = pack_bf16x2(s[8 * c8 + 2], s[8 * c8 + 3]);
+        v.z = pack_bf16x2(s[8 * c8 + 4], s[8 * c8 + 5]);
+        v.w = pack_bf16x2(s[8 * c8 + 6], s[8 * c8 + 7]);
+        *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kTileBytes + row * 128 + (((c8 & 7) ^ (row & 7)) << 4)) = v;
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, need)) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[32];
+          const uint32_t oa = tmem + kColO + cc * 32;
+          tmem_ld32(oa, r);
+          tmem_wait_ld();
+          reg_fence(r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+          tmem_st32(oa, r);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+      m_run = m_new;
+    }
+    // Unnormalised triple for each query head of the group.
+    if (T == 0) {
+      if (row < p.G) {
+        const int64_t slot = static_cast<int64_t>(qrow0 + row) * p.n_splits + c;
+        for (int e = 0; e < 128; ++e) p.part_o[slot * 128 + e] = 0.f;
+        p.part_ml[slot * 2 + 0] = -INFINITY;
+        p.part_ml[slot * 2 + 1] = 0.f;
+      }
+    } else if (ok) {
+      ok = mbar_wait(&bars->p_free, (T - 1) & 1, abort_flag, p.err, site(9));
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const int64_t slot = static_cast<int64_t>(qrow0 + row) * p.n_splits + c;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + kColO + cc * 32, r);
+          tmem_wait_ld();
+          reg_fence(r);
+          if (row < p.G) {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + slot * 128 + cc * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                                    __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
+          }
+        }
+        if (row < p.G) {
+          p.part_ml[slot * 2 + 0] = m_run;
+          p.part_ml[slot * 2 + 1] = l_run;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_gqa_tc(const DecodeTcParams& p, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(decode_gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_gqa_tc_kernel<<<dim3(p.n_splits, p.Hkv, p.B), kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

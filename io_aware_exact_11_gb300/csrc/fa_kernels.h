@@ -51,8 +51,20 @@ struct DecodeParams {
   int B, H, Nkv, n_splits, chunk;
   float scale_log2;
   unsigned int* err;
-  int Hkv = 0;    // key/value heads; 0 means H (one query head per key/value head)
-  int G = 1;      // query heads per key/value head, H = Hkv·G
+  int Hkv = 0;    // key/value heads (informational; this kernel needs Hkv = H)
+  int G = 1;      // query heads per key/value head; the CUDA-core kernel handles G = 1
+};
+
+// Grouped-query split-KV decode on tensor cores (fa_decode_tc.cu).
+struct DecodeTcParams {
+  CUtensorMap tm_q;  // q viewed as [B·Hq rows, d]: 4-D map {d, B·Hq, 1, 1}, box {64, 128, 1, 1}
+  CUtensorMap tm_k;  // {d, N, Hkv, B}, box {64, 128, 1, 1}
+  CUtensorMap tm_v;
+  float* part_o;     // [B,Hq,S,d] fp32
+  float* part_ml;    // [B,Hq,S,2] fp32
+  int B, Hq, Hkv, G, Nkv, n_splits, chunk;
+  float scale_log2;
+  unsigned int* err;
 };
 
 struct BwdParams {
@@ -80,6 +92,8 @@ struct BwdParams {
 cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_f32(int d, const FwdF32Params& p, cudaStream_t s);
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_gqa_tc(const DecodeTcParams& p, cudaStream_t s);
 cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t s, int* launches);
 
 // Size of the library-owned decode scratch (fa_decode_splitkv_noalloc).
