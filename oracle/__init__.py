@@ -8,6 +8,8 @@ from .attention import (  # noqa: F401
     attention_backward,
     attention_forward,
     attention_forward_gqa,
+    attention_decode_paged,
+    gather_pages,
     attention_probs,
     attention_rows,
     backward_delta,

@@ -39,6 +39,11 @@ Every function computes in float64.  What each one follows:
   lesson's lab takes its shapes from (Qwen2.5-7B, [Lesson] §5): query head h
   reads key/value head h // G, G = H_q / H_kv.  Written as that index map over
   the plain definition.
+* ``gather_pages`` / ``attention_decode_paged``: decode over a paged key/value
+  cache, the block-table addressing the lesson's vLLM read-along (§4) says the
+  fused kernel receives.  Logical key t of sequence b lives in page
+  block_table[b, t // bs] at slot t % bs; the oracle gathers the sequence's
+  keys in logical order and applies the plain definition.
 * ``attention_backward``: the pages give no gradient formulas, only that the
   backward recomputes S and P from Q, K, V and the saved statistics
   ([Walk] "Flash Attention Backward", [Notes] §二.5).  The oracle uses the
@@ -60,6 +65,8 @@ __all__ = [
     "attention_forward",
     "attention_rows",
     "attention_forward_gqa",
+    "gather_pages",
+    "attention_decode_paged",
     "online_attention",
     "split_partials",
     "merge_partials",
@@ -212,6 +219,38 @@ def attention_forward_gqa(q, k, v, scale: float, causal: bool = False):
     for b in range(B):
         for h in range(Hq):
             o[b, h], lse[b, h] = attention_forward(q[b, h], k[b, h // G], v[b, h // G], scale, causal=causal)
+    return o, lse
+
+
+def gather_pages(cache, block_table, seq_len: int, head: int):
+    """Logical rows [0, seq_len) of one key/value head from a paged cache.
+
+    cache [num_blocks, H_kv, bs, d]; block_table: the sequence's page ids.
+    """
+    cache = np.asarray(cache)
+    bs = cache.shape[2]
+    rows = [cache[int(block_table[t // bs]), head, t % bs] for t in range(int(seq_len))]
+    return _f64(np.stack(rows)) if rows else np.zeros((0, cache.shape[3]))
+
+
+def attention_decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: float):
+    """One query row per head against a paged cache; q [B, Hq, d].
+
+    Query head h of sequence b reads key/value head h // (Hq / H_kv) over the
+    sequence's seq_lens[b] logical keys.  Returns (O [B, Hq, d], LSE [B, Hq]).
+    """
+    q = _f64(q)
+    B, Hq, d = q.shape
+    Hkv = np.asarray(k_cache).shape[1]
+    G = Hq // Hkv
+    o = np.empty((B, Hq, d))
+    lse = np.empty((B, Hq))
+    for b in range(B):
+        for h in range(Hq):
+            k = gather_pages(k_cache, block_table[b], seq_lens[b], h // G)
+            v = gather_pages(v_cache, block_table[b], seq_lens[b], h // G)
+            ob, lb = attention_forward(q[b, h][None, :], k, v, scale)
+            o[b, h], lse[b, h] = ob[0], lb[0]
     return o, lse
 
 

@@ -364,3 +364,45 @@ def test_gqa_with_one_group_is_standard():
     k = RNG.standard_normal((1, 3, 7, 5))
     v = RNG.standard_normal((1, 3, 7, 5))
     assert np.allclose(oracle.attention_forward_gqa(q, k, v, 0.3)[0], oracle.attention_forward(q, k, v, 0.3)[0])
+
+
+# ------------------------------------------------------------ paged cache
+
+
+def _pack_pages(k, bs, order):
+    """Contiguous [B, Hkv, N, d] cache -> pages [NB, Hkv, bs, d] placed at `order`."""
+    B, Hkv, N, d = k.shape
+    per = -(-N // bs)
+    pages = np.zeros((B * per + 3, Hkv, bs, d))
+    table = np.zeros((B, per), dtype=np.int32)
+    for b in range(B):
+        for i in range(per):
+            pid = order[b * per + i]
+            blk = k[b, :, i * bs:(i + 1) * bs]
+            pages[pid, :, :blk.shape[1]] = blk
+            table[b, i] = pid
+    return pages, table
+
+
+def test_paged_decode_equals_contiguous_decode_for_any_page_order():
+    B, Hq, Hkv, N, d, bs = 2, 4, 2, 37, 8, 16
+    q = RNG.standard_normal((B, Hq, d))
+    k = RNG.standard_normal((B, Hkv, N, d))
+    v = RNG.standard_normal((B, Hkv, N, d))
+    lens = np.array([37, 21])
+    per = -(-N // bs)
+    for order in (np.arange(B * per), RNG.permutation(B * per + 3)[:B * per]):
+        kc, table = _pack_pages(k, bs, order)
+        vc, _ = _pack_pages(v, bs, order)
+        o, lse = oracle.attention_decode_paged(q, kc, vc, table, lens, 0.35)
+        for b in range(B):
+            ref_o, ref_l = oracle.attention_forward_gqa(q[b][None, :, None, :], k[b:b + 1, :, :lens[b]],
+                                                        v[b:b + 1, :, :lens[b]], 0.35)
+            assert np.allclose(o[b], ref_o[0, :, 0], atol=1e-14)
+            assert np.allclose(lse[b], ref_l[0, :, 0], atol=1e-14)
+
+
+def test_gather_pages_follows_the_block_table():
+    cache = np.arange(4 * 1 * 2 * 1, dtype=np.float64).reshape(4, 1, 2, 1)   # page p holds values 2p, 2p+1
+    rows = oracle.gather_pages(cache, [3, 0, 2], 5, 0)
+    assert rows[:, 0].tolist() == [6.0, 7.0, 0.0, 1.0, 4.0]
