@@ -373,6 +373,30 @@ def run_ours(args, ws, rank, local):
                                "frac_of_hbm_peak": kvb / t_g / 1e9 / float(peaks["hbm_gbs"])}
         del qg, kg, vg, og, lg, ws_g
 
+    if "paged" in extras:
+        # ---------------- paged cache: pages in shuffled order, every sequence 8192 keys
+        for (Hq, Hkv, S, bs) in ((32, 32, 32, 16), (28, 4, 4, 16), (28, 4, 4, 64)):
+            Bp, Np = args.decode_batch, DECODE["N"]
+            per = Np // bs
+            nb = Bp * per
+            qp = randn((Bp, Hq, 1, d), 24)
+            kp, vp = randn((nb, Hkv, bs, d), 25), randn((nb, Hkv, bs, d), 26)
+            gen.manual_seed(27)
+            table = torch.randperm(nb, generator=gen, device=dev).to(torch.int32).view(Bp, per)
+            lens = torch.full((Bp,), Np, dtype=torch.int32, device=dev)
+            op = torch.empty_like(qp)
+            lp = torch.empty((Bp, Hq), dtype=torch.float32, device=dev)
+            ws_p = torch.empty(fa.decode_workspace_size(Bp, Hq, d, S), dtype=torch.uint8, device=dev)
+            n_p = max(5, min(args.steps, 50))
+            t_p = timed(lambda: fa.decode_paged(qp, kp, vp, table, lens, n_splits=S, out=op, lse=lp, workspace=ws_p),
+                        n_p, 2) / n_p
+            kvb = 2.0 * Bp * Hkv * Np * d * 2
+            extra[f"paged_decode_{Hq}q{Hkv}kv_page{bs}"] = {
+                "workload": f"B={Bp} Hq={Hq} Hkv={Hkv} N_kv=8192 d=128 bf16, {bs}-key pages, {S} splits",
+                "hbm_gbs": kvb / t_p / 1e9, "tokens_per_s": Bp / t_p, "ms": t_p * 1e3,
+                "frac_of_hbm_peak": kvb / t_p / 1e9 / float(peaks["hbm_gbs"])}
+            del qp, kp, vp, table, lens, op, lp, ws_p
+
     if "train" in extras:
         # ---------------- training forward + backward
         Bt, Ht, Nt = TRAIN["B"], TRAIN["H"], TRAIN["N"]
@@ -460,7 +484,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
-    ap.add_argument("--extras", default="long,decode,gqa,train,causal",
+    ap.add_argument("--extras", default="long,decode,gqa,paged,train,causal",
                     help="comma list of extra workloads measured after the headline")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="decode batch B (64 is the configured workload; smaller only for profiling)")

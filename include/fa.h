@@ -140,6 +140,30 @@ FA_API fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void*
                                        int n_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_decode_paged — split-KV decode over a paged key/value cache.
+ *   The lesson's vLLM read-along (§4) notes that the fused kernel receives the
+ *   paged K/V cache together with its block tables.  Layout chosen here: each
+ *   page holds block_size consecutive keys of one key/value head,
+ *     k_cache, v_cache  [num_blocks, H_kv, block_size, d]  bf16
+ *     block_table       [B, max_blocks] int32: page ids of sequence b, in order
+ *     seq_lens          [B] int32: keys of sequence b (1 ≤ len ≤ max_blocks·block_size)
+ *   so logical key t of sequence b is row t % block_size of page
+ *   block_table[b][t / block_size].  Each sequence's keys are cut into n_splits
+ *   chunks of a multiple of 128 keys; partials are merged as in
+ *   fa_decode_splitkv.  Query heads may be grouped as in fa_decode_splitkv_gqa.
+ *   Page ids outside [0, num_blocks) and lengths outside the table are caught on
+ *   the device: page 0 is read instead, and fa_device_status then reports
+ *   FA_ERR_INVALID_ARG.  Cache slots past a sequence's end may hold anything.
+ *   q [B,H_q,1,d]; o [B,H_q,1,d]; lse [B,H_q] (or NULL); workspace as for
+ *   fa_decode_splitkv with H = H_q.
+ *   Supported: FA_BF16, d = 128, block_size ∈ {16, 32, 64, 128}, H_q = G·H_kv, G ≤ 8.
+ */
+FA_API fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                 const int32_t* seq_lens, void* o, float* lse, int B, int H_q, int H_kv,
+                                 int num_blocks, int block_size, int max_blocks, int d, fa_dtype dtype, float scale,
+                                 int n_splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fa_decode_splitkv_noalloc — fa_decode_splitkv for callers that cannot pass a
  * workspace.  The pages have no counterpart: this is a deployment variant.
  *   Who it is for: callers that cannot allocate device memory when they decode,

@@ -86,7 +86,7 @@ fa_status get_encoder(EncodeTiledFn* fn) {
 // d contiguous; box = 64 head-dim values × 128 rows, 128-byte swizzle; rows
 // past N read as zero.
 fa_status make_map(CUtensorMap* tm, const void* base, int B, int H, int N, int d, int64_t sb, int64_t sh,
-                   int64_t sn, const char* name) {
+                   int64_t sn, const char* name, int box_rows = 128) {
   EncodeTiledFn enc;
   fa_status s = get_encoder(&enc);
   if (s != FA_OK) return s;
@@ -94,7 +94,7 @@ fa_status make_map(CUtensorMap* tm, const void* base, int B, int H, int N, int d
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn) * 2, static_cast<cuuint64_t>(sh) * 2,
                            static_cast<cuuint64_t>(sb) * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -404,6 +404,101 @@ fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, voi
   return check_launch("fa_decode_splitkv_gqa", 2);
 }
 
+fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                          const int32_t* seq_lens, void* o, float* lse, int B, int H_q, int H_kv, int num_blocks,
+                          int block_size, int max_blocks, int d, fa_dtype dtype, float scale, int n_splits,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !workspace)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: null pointer");
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || num_blocks <= 0 || block_size <= 0 || max_blocks <= 0 || d <= 0 ||
+      n_splits <= 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: sizes must be positive");
+  if (H_q % H_kv != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: unknown dtype");
+  if (dtype != FA_BF16 || d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: only bf16 with d=128 is built");
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: block_size must be 16, 32, 64 or 128 (got %d)", block_size);
+  if (H_q / H_kv > 8)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: at most 8 query heads per key/value head");
+  if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: n_splits must be <= 256");
+  if (B > 65535 || H_q > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: B and H must be <= 65535");
+  if (static_cast<int64_t>(max_blocks) * block_size > (1 << 30))
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: max_blocks * block_size too large");
+  if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: scale must be finite and > 0");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: tensors must be 16-byte aligned (tables 4-byte)");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: lse must be 4-byte aligned");
+  const size_t need = fa_decode_workspace_size(B, H_q, d, n_splits);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: workspace %zu bytes, need %zu", workspace_bytes, need);
+  fa::DecodeParams p;
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.o = o;
+  p.lse = lse;
+  const size_t slots = static_cast<size_t>(B) * H_q * n_splits;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(slots * d * 4));
+  p.B = B;
+  p.H = H_q;
+  p.Nkv = 0;
+  p.n_splits = n_splits;
+  p.chunk = 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.Hkv = H_kv;
+  p.G = H_q / H_kv;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.max_blocks = max_blocks;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  fa_status r = watchdog_ptr(&p.err);
+  if (r != FA_OK) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.G == 1) {
+    cudaError_t e = fa::launch_decode_paged_bf16(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged launch");
+    return check_launch("fa_decode_paged", 2);
+  }
+  fa::DecodeTcParams t;
+  memset(&t, 0, sizeof(t));
+  const int64_t qspan = static_cast<int64_t>(B) * H_q * d;
+  if ((r = make_map(&t.tm_q, q, 1, 1, B * H_q, d, qspan, qspan, d, "q")) != FA_OK) return r;
+  // Pages as a 4-D tensor {d, block_size, H_kv, num_blocks}; one box is one page of one head.
+  const int64_t page = static_cast<int64_t>(block_size) * d;
+  if ((r = make_map(&t.tm_k, k_cache, num_blocks, H_kv, block_size, d, H_kv * page, page, d, "k_cache",
+                    block_size)) != FA_OK)
+    return r;
+  if ((r = make_map(&t.tm_v, v_cache, num_blocks, H_kv, block_size, d, H_kv * page, page, d, "v_cache",
+                    block_size)) != FA_OK)
+    return r;
+  t.block_table = block_table;
+  t.seq_lens = seq_lens;
+  t.max_blocks = max_blocks;
+  t.block_size = block_size;
+  t.num_blocks = num_blocks;
+  t.part_o = p.part_o;
+  t.part_ml = p.part_ml;
+  t.B = B;
+  t.Hq = H_q;
+  t.Hkv = H_kv;
+  t.G = p.G;
+  t.Nkv = 0;
+  t.n_splits = n_splits;
+  t.chunk = 0;
+  t.scale_log2 = p.scale_log2;
+  t.err = p.err;
+  cudaError_t e = fa::launch_decode_gqa_tc_paged(t, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged launch");
+  e = fa::launch_decode_merge(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged merge launch");
+  return check_launch("fa_decode_paged", 2);
+}
+
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N;
@@ -497,6 +592,10 @@ fa_status fa_device_status(void* stream) {
   if (code != 0) {
     const unsigned int zero = 0;
     cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if ((code & 0xFFu) == fa::kSiteBadBlock)
+      return fail(FA_ERR_INVALID_ARG, "paged decode: a block-table entry is outside [0, num_blocks) (page 0 was read)");
+    if ((code & 0xFFu) == fa::kSiteBadLength)
+      return fail(FA_ERR_INVALID_ARG, "paged decode: a sequence length is outside [1, max_blocks * block_size]");
     return fail(FA_ERR_DEVICE_TIMEOUT, "kernel %u gave up waiting at site %u", code >> 8, code & 0xFFu);
   }
   return ok();

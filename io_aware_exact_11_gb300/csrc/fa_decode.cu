@@ -28,12 +28,15 @@ constexpr int kStageBytes = 2 * kSub * kRowBytes;  // K then V: 32 KB
 constexpr int kThreads = 128;
 constexpr int kSmem = 2 * kStageBytes + 1024;
 
+constexpr int kMaxStagedPages = 256;  // page ids of a CTA's key range held in shared memory
+
 struct DecodeSmem {
   float scores[kSub];
   float probs[kSub];
   float red[8][kD];
   uint64_t full[2];
   int abort_flag;
+  int pages[kMaxStagedPages];  // paged cache only: validated page ids of this CTA's range
 };
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernDecode << 8) | s; }
@@ -47,6 +50,32 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
+// Page id of logical page `page` of sequence b, checked against the pool; an
+// out-of-range id is reported and replaced by page 0 so no address leaves it.
+__device__ __forceinline__ int checked_page(const DecodeParams& p, int b, int page) {
+  int blk = p.block_table[static_cast<int64_t>(b) * p.max_blocks + page];
+  if (blk < 0 || blk >= p.num_blocks) {
+    atomicCAS(p.err, 0u, (kKernDecode << 8) | kSiteBadBlock);
+    blk = 0;
+  }
+  return blk;
+}
+
+// Device address of logical key `t` of head h in a paged cache [num_blocks, H,
+// bs, d], and how many rows of that page follow it.  `staged` holds the ids of
+// pages page0 … page0 + kMaxStagedPages − 1; later pages are read directly.
+__device__ __forceinline__ const uint8_t* paged_row(const void* cache, const DecodeParams& p, const int* staged,
+                                                    int page0, int b, int h, int t, int* piece_rows) {
+  const int page = t / p.block_size;
+  const int slot = t - page * p.block_size;
+  const int rel = page - page0;
+  const int blk = rel < kMaxStagedPages ? staged[rel] : checked_page(p, b, page);
+  *piece_rows = p.block_size - slot;
+  return reinterpret_cast<const uint8_t*>(cache) +
+         ((static_cast<int64_t>(blk) * p.H + h) * p.block_size + slot) * kRowBytes;
+}
+
+template <bool PAGED>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
@@ -62,9 +91,26 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
   const int dchunk = lane & 15;   // 8 head-dim values per lane
   const int kpar = lane >> 4;     // which of the two keys a warp handles at once
   const int64_t bh = static_cast<int64_t>(b) * p.H + h;
-  const int key0 = c * p.chunk;
-  const int nkeys = max(0, min(p.Nkv, key0 + p.chunk) - key0);
+  int len = p.Nkv;
+  int chunk = p.chunk;
+  if (PAGED) {
+    // Per-sequence length; splits are whole 128-key multiples of it.
+    len = p.seq_lens[b];
+    if (len < 1 || len > p.max_blocks * p.block_size) {
+      if (tid == 0) atomicCAS(p.err, 0u, (kKernDecode << 8) | kSiteBadLength);
+      len = min(max(len, 1), p.max_blocks * p.block_size);
+    }
+    chunk = (((len + p.n_splits - 1) / p.n_splits) + 127) & ~127;
+  }
+  const int key0 = c * chunk;
+  const int nkeys = max(0, min(len, key0 + chunk) - key0);
   const int nsub = (nkeys + kSub - 1) / kSub;
+  const int page0 = PAGED ? key0 / max(p.block_size, 1) : 0;
+  if (PAGED && nkeys > 0) {
+    // Stage this range's page ids with one coalesced, checked load.
+    const int npages = min(kMaxStagedPages, (key0 + nkeys - 1) / p.block_size - page0 + 1);
+    for (int i = tid; i < npages; i += kThreads) sm.pages[i] = checked_page(p, b, page0 + i);
+  }
 
   const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k) + (bh * p.Nkv + key0) * kRowBytes;
   const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v) + (bh * p.Nkv + key0) * kRowBytes;
@@ -81,9 +127,22 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     const int n = min(kSub, nkeys - i * kSub);
     const uint32_t bytes = static_cast<uint32_t>(n) * kRowBytes;
     mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
-    bulk_load(ring + st * kStageBytes, kbase + static_cast<int64_t>(i) * kSub * kRowBytes, bytes, &sm.full[st]);
-    bulk_load(ring + st * kStageBytes + kSub * kRowBytes, vbase + static_cast<int64_t>(i) * kSub * kRowBytes,
-              bytes, &sm.full[st]);
+    if (!PAGED) {
+      bulk_load(ring + st * kStageBytes, kbase + static_cast<int64_t>(i) * kSub * kRowBytes, bytes, &sm.full[st]);
+      bulk_load(ring + st * kStageBytes + kSub * kRowBytes, vbase + static_cast<int64_t>(i) * kSub * kRowBytes,
+                bytes, &sm.full[st]);
+    } else {
+      // One copy per page piece: pages hold block_size contiguous rows of one head.
+      for (int r = 0; r < n;) {
+        int rows;
+        const uint8_t* ksrc = paged_row(p.k, p, sm.pages, page0, b, h, key0 + i * kSub + r, &rows);
+        const uint8_t* vsrc = paged_row(p.v, p, sm.pages, page0, b, h, key0 + i * kSub + r, &rows);
+        rows = min(rows, n - r);
+        bulk_load(ring + st * kStageBytes + r * kRowBytes, ksrc, rows * kRowBytes, &sm.full[st]);
+        bulk_load(ring + st * kStageBytes + kSub * kRowBytes + r * kRowBytes, vsrc, rows * kRowBytes, &sm.full[st]);
+        r += rows;
+      }
+    }
   };
   if (tid == 0) {
     if (nsub > 0) issue(0);
@@ -212,6 +271,17 @@ __global__ void __launch_bounds__(kD) decode_merge_kernel(const DecodeParams p) 
 
 }  // namespace
 
+cudaError_t launch_decode_paged_bf16(const DecodeParams& p, cudaStream_t stream) {
+  if (p.G != 1) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<true><<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
   decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
   return cudaGetLastError();
@@ -219,9 +289,9 @@ cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t stream) {
   if (d != kD || p.G != 1) return cudaErrorInvalidValue;  // groups go to the tensor-core kernel
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
+  decode_split_kernel<false><<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);

@@ -18,6 +18,13 @@
 // owner and MMA issuer.  TMEM: S buffers at columns 0 and 128, O at 256.
 // Rows keep their reference max until a tile's max exceeds it by 2^8 (base 2),
 // exactly as in the forward kernel; the merge accepts any reference m.
+//
+// Paged cache (PAGED): k and v are [num_blocks, H_kv, bs, d] with bs dividing
+// 128; logical key t of sequence b is row t % bs of page block_table[b][t / bs].
+// Each 128-key tile is loaded as 128/bs page boxes; pages past the sequence are
+// requested at an out-of-range row so TMA fills them with zeros, and on a
+// split's last, partial tile the softmax warp zeroes the V rows past the end
+// (slots of a partly filled page hold stale data) before P̃V runs.
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -36,7 +43,9 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kOffQ = 0;
 constexpr int kOffR = kOffQ + kSlot;
 constexpr int kOffP = kOffR + kRing * kSlot;
-constexpr int kOffBar = kOffP + kSlot;
+constexpr int kOffPages = kOffP + kSlot;       // paged cache: staged page ids
+constexpr int kMaxStagedPages = 1024;
+constexpr int kOffBar = kOffPages + kMaxStagedPages * 4;
 constexpr int kSmem = kOffBar + 256 + 1024;
 
 struct Bars {
@@ -54,6 +63,7 @@ __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernDeco
 __device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int seq_v(int j, int T) { return min(2 * j + 2, 2 * T - 1); }
 
+template <bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid_constant__ DecodeTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -67,8 +77,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
   const int hkv = blockIdx.y;
   const int b = blockIdx.z;
   const int qrow0 = b * p.Hq + hkv * p.G;  // first query row in the [B·H_q, d] view
-  const int key0 = c * p.chunk;
-  const int kend = min(p.Nkv, key0 + p.chunk);
+  int len = p.Nkv;
+  int chunk = p.chunk;
+  if (PAGED) {
+    len = p.seq_lens[b];
+    if (len < 1 || len > p.max_blocks * p.block_size) {
+      if (threadIdx.x == 0) atomicCAS(p.err, 0u, (kKernDecode << 8) | kSiteBadLength);
+      len = min(max(len, 1), p.max_blocks * p.block_size);
+    }
+    chunk = (((len + p.n_splits - 1) / p.n_splits) + 127) & ~127;
+  }
+  const int key0 = c * chunk;
+  const int kend = min(len, key0 + chunk);
   const int nkeys = max(0, kend - key0);
   const int T = (nkeys + kBN - 1) / kBN;
 
@@ -99,6 +119,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
 
   if (warp == 1) {
     // ------------------------------------------------------------ producer
+    int* staged = reinterpret_cast<int*>(smem + kOffPages);
+    const int page0 = PAGED ? key0 / p.block_size : 0;
+    if (PAGED && T > 0) {
+      // The warp stages this range's page ids with one coalesced, checked load.
+      const int npages = min(kMaxStagedPages, (kend - 1) / p.block_size - page0 + 1);
+      for (int i = lane; i < npages; i += 32) {
+        int blk = p.block_table[static_cast<int64_t>(b) * p.max_blocks + page0 + i];
+        if (blk < 0 || blk >= p.num_blocks) {
+          atomicCAS(p.err, 0u, (kKernDecode << 8) | kSiteBadBlock);
+          blk = 0;
+        }
+        staged[i] = blk;
+      }
+      __syncwarp();
+    }
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
@@ -119,9 +154,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
         mbar_arrive_expect_tx(&bars->r_full[slot], kSlot);
         const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
-                      key0 + jt * kBN, hkv, b);
+        if (!PAGED) {
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
+                        key0 + jt * kBN, hkv, b);
+        } else {
+          const int bs = p.block_size;
+          for (int pg = 0; pg < kBN / bs; ++pg) {
+            const int t0 = key0 + jt * kBN + pg * bs;  // a multiple of bs
+            int blk = 0, row = 0;
+            if (t0 < kend) {
+              const int rel = t0 / bs - page0;
+              if (rel < kMaxStagedPages) {
+                blk = staged[rel];
+              } else {
+                blk = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t0 / bs];
+                if (blk < 0 || blk >= p.num_blocks) {
+                  atomicCAS(p.err, 0u, (kKernDecode << 8) | kSiteBadBlock);
+                  blk = 0;
+                }
+              }
+            } else {
+              row = bs;  // wholly out of range: zero fill
+            }
+            for (int kb = 0; kb < 2; ++kb)
+              tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes + pg * bs * 128, tm, &bars->r_full[slot],
+                          kb * 64, row, hkv, blk);
+          }
+        }
         ++issued;
       }
       if (*abort_flag) {
@@ -270,6 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         }
         tmem_wait_st();
       }
+      if (PAGED && valid < kBN) {
+        // Zero the V rows past the sequence end once V_j has landed.
+        const int t = seq_v(j, T);
+        ok = mbar_wait(&bars->r_full[t % kRing], (t / kRing) & 1, abort_flag, p.err, site(10));
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        uint8_t* vt = smem + kOffR + (t % kRing) * kSlot;
+        for (int rr = max(valid, 0) + lane; rr < kBN; rr += 32)
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vt + kb * kTileBytes + rr * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
@@ -321,9 +394,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
 }  // namespace
 
 cudaError_t launch_decode_gqa_tc(const DecodeTcParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_gqa_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  decode_gqa_tc_kernel<<<dim3(p.n_splits, p.Hkv, p.B), kThreads, kSmem, stream>>>(p);
+  decode_gqa_tc_kernel<false><<<dim3(p.n_splits, p.Hkv, p.B), kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_gqa_tc_paged(const DecodeTcParams& p, cudaStream_t stream) {
+  if (p.block_size < 16 || p.block_size > kBN || (kBN % p.block_size) != 0) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_gqa_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_gqa_tc_kernel<true><<<dim3(p.n_splits, p.Hkv, p.B), kThreads, kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

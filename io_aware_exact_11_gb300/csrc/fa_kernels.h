@@ -53,13 +53,23 @@ struct DecodeParams {
   unsigned int* err;
   int Hkv = 0;    // key/value heads (informational; this kernel needs Hkv = H)
   int G = 1;      // query heads per key/value head; the CUDA-core kernel handles G = 1
+  // Paged cache (k, v are [num_blocks, H, block_size, d]); null block_table = contiguous.
+  const int* block_table = nullptr;  // [B, max_blocks]
+  const int* seq_lens = nullptr;     // [B]
+  int max_blocks = 0, block_size = 0, num_blocks = 0;
 };
+
+// Device-side argument checks report through the status word with these sites.
+enum : unsigned int { kSiteBadBlock = 0xE1, kSiteBadLength = 0xE2 };
 
 // Grouped-query split-KV decode on tensor cores (fa_decode_tc.cu).
 struct DecodeTcParams {
   CUtensorMap tm_q;  // q viewed as [B·Hq rows, d]: 4-D map {d, B·Hq, 1, 1}, box {64, 128, 1, 1}
-  CUtensorMap tm_k;  // {d, N, Hkv, B}, box {64, 128, 1, 1}
+  CUtensorMap tm_k;  // {d, N, Hkv, B}, box {64, 128, 1, 1}; paged: {d, bs, Hkv, num_blocks}, box {64, bs, 1, 1}
   CUtensorMap tm_v;
+  const int* block_table;  // paged cache only: [B, max_blocks]
+  const int* seq_lens;     // paged cache only: [B]
+  int max_blocks, block_size, num_blocks;
   float* part_o;     // [B,Hq,S,d] fp32
   float* part_ml;    // [B,Hq,S,2] fp32
   int B, Hq, Hkv, G, Nkv, n_splits, chunk;
@@ -94,6 +104,8 @@ cudaError_t launch_fwd_f32(int d, const FwdF32Params& p, cudaStream_t s);
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_gqa_tc(const DecodeTcParams& p, cudaStream_t s);
+cudaError_t launch_decode_paged_bf16(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_gqa_tc_paged(const DecodeTcParams& p, cudaStream_t s);
 cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t s, int* launches);
 
 // Size of the library-owned decode scratch (fa_decode_splitkv_noalloc).

@@ -27,6 +27,7 @@ EXPORTED = (
     "fa_decode_workspace_size",
     "fa_decode_splitkv",
     "fa_decode_splitkv_gqa",
+    "fa_decode_paged",
     "fa_decode_splitkv_noalloc",
     "fa_backward_workspace_size",
     "fa_backward",
@@ -67,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.fa_decode_splitkv.restype = i32
         L.fa_decode_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
         L.fa_decode_splitkv_gqa.restype = i32
+        L.fa_decode_paged.argtypes = [vp] * 7 + [i32] * 8 + [f32, i32, vp, sz, vp]
+        L.fa_decode_paged.restype = i32
         L.fa_backward_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fa_backward_workspace_size.restype = sz
         L.fa_backward.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, vp, sz, vp]
@@ -222,6 +225,40 @@ def decode_splitkv_gqa(q, k, v, n_splits: int = 32, scale: float | None = None, 
     _check(lib().fa_decode_splitkv_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nkv, d,
                                        _dtype_code(q), float(scale), int(n_splits), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, n_splits: int = 8, scale: float | None = None,
+                 out=None, lse=None, workspace=None, stream=None):
+    """Split-KV decode over a paged cache.
+
+    q [B,Hq,1,d]; k_cache/v_cache [num_blocks, Hkv, block_size, d]; block_table
+    [B, max_blocks] int32; seq_lens [B] int32 (device tensors).
+    """
+    torch = _torch()
+    _check_cuda(q, k_cache, v_cache, block_table, seq_lens)
+    B, Hq, one, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if one != 1 or d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("paged decode inputs must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, 1, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(B, Hq, d, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out),
+                                 _ptr(lse), B, Hq, Hkv, NB, bs, block_table.shape[1], d, _dtype_code(q), float(scale),
+                                 int(n_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)))
     return out, lse
 
 

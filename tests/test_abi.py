@@ -144,3 +144,15 @@ def test_gqa_decode_validates_before_cuda(L):
     assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
     assert dec(wsb=64) == fa.FA_ERR_INVALID_ARG
     assert b"workspace" in L.fa_get_last_error()
+
+
+def test_paged_decode_validates_before_cuda(L):
+    def dec(bs=16, Hq=28, Hkv=4, d=128, wsb=1 << 24, table=FAKE):
+        return L.fa_decode_paged(FAKE, FAKE, FAKE, table, FAKE, FAKE, None, 2, Hq, Hkv, 100, bs, 64, d, fa.FA_BF16,
+                                 0.1, 8, FAKE, wsb, None)
+    assert dec(bs=24) == fa.FA_ERR_UNSUPPORTED
+    assert dec(bs=256) == fa.FA_ERR_UNSUPPORTED
+    assert dec(Hq=30) == fa.FA_ERR_INVALID_ARG
+    assert dec(table=None) == fa.FA_ERR_INVALID_ARG
+    assert dec(wsb=16) == fa.FA_ERR_INVALID_ARG
+    assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
