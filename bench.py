@@ -418,6 +418,24 @@ def run_ours(args, ws, rank, local):
                                            "unit": "TFLOP/s", "frac": 2.5 * ff / t_b / 1e12 / peak,
                                            "kernel": "time: whole backward (3 kernels); traffic: bwd_main_kernel",
                                            "traffic": traffic_for("bwd_train", ("fa_bwd.cu", "sm103.cuh"))}}
+    if "fp8" in extras:
+        # ---------------- FP8 (E4M3) forward at the prefill shape; peak = measured bf16 × the nominal 2x
+        Bf, Hf, Nf = PREFILL["B"], PREFILL["H"], PREFILL["N"]
+        q8, k8, v8 = (randn((Bf, Hf, Nf, d), s).float().to(torch.float8_e4m3fn).view(torch.uint8)
+                      for s in (28, 29, 30))
+        of = torch.empty((Bf, Hf, Nf, d), dtype=torch.bfloat16, device=dev)
+        lf = torch.empty((Bf, Hf, Nf), dtype=torch.float32, device=dev)
+        n_f = max(5, min(args.steps, 50))
+        t_f8 = timed(lambda: fa.forward_fp8(q8, k8, v8, out=of, lse=lf), n_f, 2) / n_f
+        ff8 = fwd_flops(Bf, Hf, Nf, d)
+        peak8 = 2.0 * peak
+        extra["fp8_prefill_fwd"] = {"workload": "B=4 H=32 N=4096 d=128 E4M3 in, bf16 out",
+                                    "tflops": ff8 / t_f8 / 1e12, "ms": t_f8 * 1e3,
+                                    "roofline": {"bound": "tensor", "achieved": ff8 / t_f8 / 1e12, "peak": peak8,
+                                                 "unit": "TFLOP/s", "frac": ff8 / t_f8 / 1e12 / peak8,
+                                                 "peak_source": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)"}}
+        del q8, k8, v8, of, lf
+
     if "causal" in extras:
         # ---------------- causal mask: prefill forward and training backward
         Bc, Hc, Nc = PREFILL["B"], PREFILL["H"], PREFILL["N"]
@@ -484,7 +502,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
-    ap.add_argument("--extras", default="long,decode,gqa,paged,train,causal",
+    ap.add_argument("--extras", default="long,decode,gqa,paged,train,causal,fp8",
                     help="comma list of extra workloads measured after the headline")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="decode batch B (64 is the configured workload; smaller only for profiling)")

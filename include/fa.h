@@ -98,6 +98,19 @@ FA_API fa_status fa_forward_masked(const void* q, const void* k, const void* v, 
                                    const int64_t* strides, fa_mask mask, void* stream);
 
 /*
+ * fa_forward_fp8 — forward with FP8 (E4M3) inputs, FlashAttention-3's addition
+ *   (lesson §3.3; interview notes §四.5).  q, k, v hold E4M3 codes (one byte
+ *   each, [B,H,N,d] contiguous) whose true values are q_descale·q, k_descale·k,
+ *   v_descale·v; the MMAs run as tcgen05 kind::f8f6f4 with fp32 accumulation,
+ *   P̃ is rounded to E4M3 for the P̃V product while ℓ sums the unrounded fp32
+ *   values, and o is written as bf16 [B,H,N_q,d] with lse fp32 as in fa_forward.
+ *   mask: FA_MASK_NONE or FA_MASK_CAUSAL.  Supported: d = 128.
+ */
+FA_API fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int N_q, int N_kv, int d, float scale, float q_descale,
+                                float k_descale, float v_descale, fa_mask mask, void* stream);
+
+/*
  * fa_decode_workspace_size — bytes of workspace fa_decode_splitkv needs:
  *   the partial outputs B·H·n_splits·d·4 bytes and the partial (m, ℓ) pairs
  *   B·H·n_splits·2·4 bytes, each rounded up to a multiple of 256.

@@ -86,17 +86,20 @@ fa_status get_encoder(EncodeTiledFn* fn) {
 // d contiguous; box = 64 head-dim values × 128 rows, 128-byte swizzle; rows
 // past N read as zero.
 fa_status make_map(CUtensorMap* tm, const void* base, int B, int H, int N, int d, int64_t sb, int64_t sh,
-                   int64_t sn, const char* name, int box_rows = 128) {
+                   int64_t sn, const char* name, int box_rows = 128, bool fp8 = false) {
   EncodeTiledFn enc;
   fa_status s = get_encoder(&enc);
   if (s != FA_OK) return s;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn) * 2, static_cast<cuuint64_t>(sh) * 2,
-                           static_cast<cuuint64_t>(sb) * 2};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  // One box row is 128 bytes (the swizzle width): 64 bf16 or 128 E4M3 values.
+  const int esz = fp8 ? 1 : 2;
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn) * esz, static_cast<cuuint64_t>(sh) * esz,
+                           static_cast<cuuint64_t>(sb) * esz};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = enc(tm, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
@@ -190,6 +193,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     p.o_sn = st[11];
     p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal;
+    p.o_scale = 1.f;
     cudaError_t e = fa::launch_fwd_bf16(d, p, s);
     if (e != cudaSuccess) return cuda_fail(e, "fa_forward launch");
     return check_launch("fa_forward", 1);
@@ -231,6 +235,50 @@ fa_status fa_forward_masked(const void* q, const void* k, const void* v, void* o
     return fail(FA_ERR_INVALID_ARG, "fa_forward_masked: unknown mask %d", static_cast<int>(mask));
   return forward_impl(q, k, v, o, lse, B, H, N_q, N_kv, d, dtype, scale, strides, mask == FA_MASK_CAUSAL ? 1 : 0,
                       stream);
+}
+
+fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                         int N_kv, int d, float scale, float q_descale, float k_descale, float v_descale,
+                         fa_mask mask, void* stream) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: null tensor pointer");
+  if (B <= 0 || H <= 0 || N_q <= 0 || N_kv <= 0 || d <= 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: sizes must be positive");
+  if (mask != FA_MASK_NONE && mask != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: unknown mask %d", static_cast<int>(mask));
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp8: only d=128 is built (got %d)", d);
+  if (bad_scale(scale) || bad_scale(q_descale) || bad_scale(k_descale) || bad_scale(v_descale))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: scale and descale factors must be finite and > 0");
+  if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp8: B and H must be <= 65535");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: q, k, v, o must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: lse must be 4-byte aligned");
+  if (mask == FA_MASK_CAUSAL && N_q > N_kv)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: causal attention needs N_q <= N_kv");
+  fa::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int64_t nq = static_cast<int64_t>(N_q) * d, nk = static_cast<int64_t>(N_kv) * d;
+  fa_status r;
+  if ((r = make_map(&p.tm_q, q, B, H, N_q, d, H * nq, nq, d, "q", 128, true)) != FA_OK) return r;
+  if ((r = make_map(&p.tm_k, k, B, H, N_kv, d, H * nk, nk, d, "k", 128, true)) != FA_OK) return r;
+  if ((r = make_map(&p.tm_v, v, B, H, N_kv, d, H * nk, nk, d, "v", 128, true)) != FA_OK) return r;
+  if ((r = watchdog_ptr(&p.err)) != FA_OK) return r;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Nq = N_q;
+  p.Nkv = N_kv;
+  p.o_sb = H * nq;
+  p.o_sh = nq;
+  p.o_sn = d;
+  // True scores are q_descale·k_descale·(Q₈K₈ᵀ); true O is v_descale·(P̃V₈)/ℓ.
+  p.scale_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  p.o_scale = v_descale;
+  p.causal = mask == FA_MASK_CAUSAL ? 1 : 0;
+  cudaError_t e = fa::launch_fwd_fp8(d, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_forward_fp8 launch");
+  return check_launch("fa_forward_fp8", 1);
 }
 
 size_t fa_decode_workspace_size(int B, int H, int d, int n_splits) {

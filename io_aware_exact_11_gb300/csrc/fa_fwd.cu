@@ -32,11 +32,19 @@
 // last row can see; rows mask the rest of their diagonal tile with −∞, and
 // the heaviest query blocks are scheduled first.
 //
+// FP8 (E4M3) variant, FlashAttention-3's addition noted in the lesson (§3.3) and
+// the interview notes (§四.5): Q, K, V arrive as E4M3 with per-tensor descale
+// factors, the MMAs run as kind::f8f6f4 (32 elements per instruction, still 32
+// bytes per k-step), P̃ is written as E4M3 (lazy rescaling keeps it <= 256, inside
+// E4M3's ±448) and ℓ sums the unrounded fp32 values; O leaves as bf16.
+//
 // Lazy rescaling: a row keeps its reference max m until a tile's max exceeds
 // it by more than kRescaleLog2 (base-2 units).  Until then P̃ = 2^(σ'S − m) is
 // at most 2^kRescaleLog2 and O, ℓ keep accumulating against the same m, so the
 // final O/ℓ and LSE = m + ln ℓ are the same numbers in exact arithmetic; only
 // when the max really moves is O rescaled in TMEM by e^(m_old − m_new).
+#include <cuda_fp8.h>
+
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -52,15 +60,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+template <int D, bool FP8>
 struct FwdLayout {
-  static constexpr int kNKB = D / 64;               // 128-byte blocks along the head dim
-  static constexpr int kSlot = kNKB * kTileBytes;   // one Q, K or V tile
+  static constexpr int kEB = FP8 ? 1 : 2;            // bytes per element
+  static constexpr int kNKB = D * kEB / 128;         // 128-byte blocks along the head dim
+  static constexpr int kSlot = kNKB * kTileBytes;    // one Q, K or V tile
+  static constexpr int kPB = kBN * kEB / 128;        // 128-byte blocks of one P̃ row
+  static constexpr int kStepK = 32 / kEB;            // elements per MMA k-step (32 bytes)
   static constexpr int kRing = 3;                   // K_j, V_j, K_{j+1} in flight
   static constexpr int kQ = 0;
   static constexpr int kR = kQ + kQT * kSlot;
   static constexpr int kP = kR + kRing * kSlot;     // one P̃ tile per query tile
-  static constexpr int kBar = kP + kQT * 2 * kTileBytes;
+  static constexpr int kBar = kP + kQT * kPB * kTileBytes;
   static constexpr int kUsed = kBar + 512;
   // +1 KB so the base can be rounded up to 1024; at least 120 KB so only one
   // CTA (which owns all 512 TMEM columns) is resident per SM.
@@ -79,15 +90,23 @@ struct FwdBars {
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernFwd << 8) | s; }
 
+// Four fp32 values -> four E4M3 bytes (round to nearest even, saturating), the
+// first value in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 // Position in the load sequence K_0, K_1, V_0, K_2, V_1, K_3, …, V_{T−1}: keys run
 // one tile ahead of values, which is also the order the MMA warp consumes them
 // (S(j) needs K_j; P̃(j−1)V_{j−1} is issued right after it).
 __device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int seq_v(int j, int T) { return min(2 * j + 2, 2 * T - 1); }
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -169,8 +188,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
+      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t kIdescO = FP8 ? idesc_e4m3_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
+      auto mma = [&](uint32_t dst, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
+        if (FP8)
+          mma_e4m3_ss(dst, ad, bd, id, acc);
+        else
+          mma_bf16_ss(dst, ad, bd, id, acc);
+      };
       const uint32_t sQ = smem_u32(smem + L::kQ);
       const uint32_t sR = smem_u32(smem + L::kR);
       const uint32_t sP = smem_u32(smem + L::kP);
@@ -182,13 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         for (int i = 0; i < kQT; ++i) {
           if (!mbar_wait(&bars->p_full[i], jj & 1, abort_flag, p.err, site(4))) return false;
           tc_fence_after();
-          const uint32_t pbuf = sP + i * 2 * kTileBytes;
+          const uint32_t pbuf = sP + i * L::kPB * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
+          for (int kk = 0; kk < kBN / L::kStepK; ++kk) {
             // A = P̃_i (K-major, keys along K); B = V_j (MN-major: head dim contiguous).
             const uint64_t ad = sdesc_sw128(pbuf + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTileBytes, 1024);
-            mma_bf16_ss(tmem + kColO + i * 128, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(vb + kk * L::kStepK * 128, kTileBytes, 1024);
+            mma(tmem + kColO + i * 128, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->p_free[i]);
         }
@@ -206,10 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
           tc_fence_after();
           const uint32_t qb = sQ + i * L::kSlot;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < D / L::kStepK; ++kk) {
             const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-            mma_bf16_ss(tmem + i * kBN, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                        kIdescS, kk > 0 ? 1u : 0u);
+            mma(tmem + i * kBN, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescS,
+                kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[i]);
         }
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     const uint32_t s_col = qt * kBN;
     const uint32_t o_col = kColO + qt * 128;
     const float sl2 = p.scale_log2;
-    uint8_t* pbuf = smem + L::kP + qt * 2 * kTileBytes;
+    uint8_t* pbuf = smem + L::kP + qt * L::kPB * kTileBytes;
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
@@ -301,16 +326,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       // P̃_i and O_i are free once the P̃_i V MMA of tile j−1 has finished.
       ok = mbar_wait(&bars->p_free[qt], (j & 1) ^ 1, abort_flag, p.err, site(9));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (FP8) {
+        // 16 keys per 16-byte chunk, one 128-byte block per row.
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint4 v;
-        v.x = pack_bf16x2(s[8 * c8 + 0], s[8 * c8 + 1]);
-        v.y = pack_bf16x2(s[8 * c8 + 2], s[8 * c8 + 3]);
-        v.z = pack_bf16x2(s[8 * c8 + 4], s[8 * c8 + 5]);
-        v.w = pack_bf16x2(s[8 * c8 + 6], s[8 * c8 + 7]);
-        const int kb = c8 >> 3;
-        const int cc = c8 & 7;
-        *reinterpret_cast<uint4*>(pbuf + kb * kTileBytes + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 v;
+          v.x = pack_e4m3x4(s[16 * cc + 0], s[16 * cc + 1], s[16 * cc + 2], s[16 * cc + 3]);
+          v.y = pack_e4m3x4(s[16 * cc + 4], s[16 * cc + 5], s[16 * cc + 6], s[16 * cc + 7]);
+          v.z = pack_e4m3x4(s[16 * cc + 8], s[16 * cc + 9], s[16 * cc + 10], s[16 * cc + 11]);
+          v.w = pack_e4m3x4(s[16 * cc + 12], s[16 * cc + 13], s[16 * cc + 14], s[16 * cc + 15]);
+          *reinterpret_cast<uint4*>(pbuf + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+        }
+      } else {
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
+          uint4 v;
+          v.x = pack_bf16x2(s[8 * c8 + 0], s[8 * c8 + 1]);
+          v.y = pack_bf16x2(s[8 * c8 + 2], s[8 * c8 + 3]);
+          v.z = pack_bf16x2(s[8 * c8 + 4], s[8 * c8 + 5]);
+          v.w = pack_bf16x2(s[8 * c8 + 6], s[8 * c8 + 7]);
+          const int kb = c8 >> 3;
+          const int cc = c8 & 7;
+          *reinterpret_cast<uint4*>(pbuf + kb * kTileBytes + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+        }
       }
       // Rescale the running output only when some row of this warp moved its
       // reference max.
@@ -338,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       ok = mbar_wait(&bars->p_free[qt], (T - 1) & 1, abort_flag, p.err, site(10));
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const float inv = 1.f / l_run;
+        const float inv = p.o_scale / l_run;
         const int grow = m0 + qt * kBM + row;
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + b * p.o_sb + h * p.o_sh +
                               static_cast<int64_t>(grow) * p.o_sn;
@@ -374,21 +412,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   }
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
-  using L = FwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  using L = FwdLayout<D, FP8>;
+  cudaError_t e =
+      cudaFuncSetAttribute(fwd_bf16_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((p.Nq + kQT * kBM - 1) / (kQT * kBM), p.H, p.B);
-  fwd_bf16_kernel<D><<<grid, kThreads, L::kSmem, stream>>>(p);
+  fwd_bf16_kernel<D, FP8><<<grid, kThreads, L::kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch_impl<128>(p, stream);
-  if (d == 64) return launch_impl<64>(p, stream);
+  if (d == 128) return launch_impl<128, false>(p, stream);
+  if (d == 64) return launch_impl<64, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_fp8(int d, const FwdParams& p, cudaStream_t stream) {
+  if (d == 128) return launch_impl<128, true>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -23,9 +23,10 @@ struct FwdParams {
   float* lse;  // may be null
   int B, H, Nq, Nkv;
   int64_t o_sb, o_sh, o_sn;  // element strides of O
-  float scale_log2;          // σ·log2(e)
+  float scale_log2;          // σ·log2(e) (FP8: also × the Q and K descale factors)
   int causal;                // query i sees keys j <= i + (Nkv − Nq); needs Nq <= Nkv
   unsigned int* err;
+  float o_scale = 1.f;       // multiplies O before the 1/ℓ (FP8: the V descale factor)
 };
 
 struct FwdF32Params {
@@ -100,6 +101,7 @@ struct BwdParams {
 };
 
 cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_fp8(int d, const FwdParams& p, cudaStream_t s);  // E4M3 Q/K/V, bf16 O
 cudaError_t launch_fwd_f32(int d, const FwdF32Params& p, cudaStream_t s);
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t s);

@@ -24,6 +24,7 @@ EXPORTED = (
     "fa_abi_version",
     "fa_forward",
     "fa_forward_masked",
+    "fa_forward_fp8",
     "fa_decode_workspace_size",
     "fa_decode_splitkv",
     "fa_decode_splitkv_gqa",
@@ -62,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.fa_forward.restype = i32
         L.fa_forward_masked.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp]
         L.fa_forward_masked.restype = i32
+        L.fa_forward_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32, f32, i32, vp]
+        L.fa_forward_fp8.restype = i32
         L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fa_decode_workspace_size.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
@@ -167,6 +170,29 @@ def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse:
     else:
         _check(lib().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d,
                                 _dtype_code(q), float(scale), strides, _stream_ptr(stream)))
+    return out, lse
+
+
+def forward_fp8(q8, k8, v8, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
+                scale: float | None = None, out=None, lse=None, causal: bool = False, stream=None):
+    """FP8 forward.  q8/k8/v8: uint8 tensors of E4M3 codes [B,H,N,d] (or torch
+    float8_e4m3fn); true values are descale × code value.  Returns (O bf16, LSE)."""
+    torch = _torch()
+    _check_cuda(q8, k8, v8)
+    B, H, Nq, d = q8.shape
+    Nkv = k8.shape[2]
+    for t in (q8, k8, v8):
+        if t.element_size() != 1 or not t.is_contiguous():
+            raise ValueError("fp8 inputs must be contiguous one-byte tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    _check(lib().fa_forward_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d, float(scale),
+                                float(q_descale), float(k_descale), float(v_descale),
+                                FA_MASK_CAUSAL if causal else FA_MASK_NONE, _stream_ptr(stream)))
     return out, lse
 
 

@@ -40,6 +40,41 @@ def bf16_bits_to_f32(u: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(u, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities; finite values saturate at ±448), nearest-even.  Returns
+    uint8 codes.  Used to build FP8 inputs; the oracle reads them back with
+    ``e4m3_bits_to_f32``."""
+    x = np.asarray(x, dtype=np.float32)
+    sign = (np.signbit(x)).astype(np.uint8) << 7
+    a = np.minimum(np.abs(x).astype(np.float64), 448.0)
+    out = np.zeros(a.shape, dtype=np.uint8)
+    # Normal range: exponent e in [-6, 8], value = 2^e · (1 + m/8).
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)
+    step = np.exp2(e - 3)                       # spacing of representable values
+    q = np.round(a / step) * step               # np.round is half-to-even
+    # Rounding can carry into the next binade; recompute its exponent.
+    e2 = np.floor(np.log2(np.where(q > 0, q, 1.0)))
+    normal = q >= 2.0 ** -6
+    mant = np.where(normal, np.round(q / np.exp2(e2) * 8) - 8, np.round(q / 2.0 ** -9))
+    expf = np.where(normal, e2 + 7, 0)
+    code = (expf.astype(np.int64) << 3) | mant.astype(np.int64)
+    out[...] = np.where(a > 0, code, 0).astype(np.uint8)
+    return out | sign
+
+
+def e4m3_bits_to_f32(u: np.ndarray) -> np.ndarray:
+    """Exact value of FP8 E4M3 codes (uint8) as float32 (the NaN code maps to NaN)."""
+    u = np.asarray(u, dtype=np.uint8).astype(np.int64)
+    s = np.where(u & 0x80, -1.0, 1.0)
+    e = (u >> 3) & 0xF
+    m = u & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 0xF) & (m == 0x7), np.nan, val)
+    return (s * val).astype(np.float32)
+
+
 def _threads() -> int:
     return max(1, min(16, len(os.sched_getaffinity(0))))
 

@@ -1,0 +1,111 @@
+"""GPU parity of the FP8 (E4M3) forward against the float64 oracle.
+
+The oracle reads the dequantized inputs (descale × E4M3 value), so only the
+kernel's own arithmetic is measured.  Scores are products of E4M3 values
+(exact in fp32) summed in fp32.  The bound is derived from the two roundings
+the kernel adds: P̃ is rounded to E4M3 before P̃V (relative error <= 2^-4 in the
+normal range, absolute error <= 2^-10 below it, in units where the row max of
+P̃ is >= 1) and O is stored as bf16 (<= 2^-9 relative).  Per element:
+  |ΔO_rt| <= 2^-4·Σ_j P_rj|v_jt| + 2^-10·Σ_j |v_jt| / ℓ_r + 2^-9·|O_rt| + 1e-4,
+with P the exact probabilities and ℓ_r = Σ_j e^(s_rj − max_j s_rj).  LSE is
+summed in fp32 from the unrounded values: within 1e-3.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_exact_11_gb300 import fa, inputs
+from tests.gpu_helpers import cpu64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.lib()
+    yield
+    fa.device_status()
+
+
+def _quant(seed, name, B, H, N, d, descale):
+    x = inputs.normal_tensor(seed, name, B, H, N, d, "fp32")
+    codes = inputs.f32_to_e4m3_bits(x / descale)
+    return codes, inputs.e4m3_bits_to_f32(codes).astype(np.float64) * descale
+
+
+def _bound(q, k, v, scale, causal, rows=None):
+    """Elementwise error bound for the rows of one head (see module docstring)."""
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows)
+    s = scale * (q[rows] @ k.T)
+    if causal:
+        s = np.where(oracle.causal_visible(rows, q.shape[0], k.shape[0]), s, -np.inf)
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    ell = e.sum(axis=1)
+    P = e / ell[:, None]
+    o = P @ v
+    vis = np.isfinite(s).astype(np.float64)
+    return 2.0 ** -4 * (P @ np.abs(v)) + 2.0 ** -10 * (vis @ np.abs(v)) / ell[:, None] + 2.0 ** -9 * np.abs(o) + 1e-4
+
+
+def _check(seed, B, H, Nq, Nkv, causal=False, descales=(1.0, 1.0, 1.0), sample=None):
+    import torch
+    d = 128
+    qc, qf = _quant(seed, "q", B, H, Nq, d, descales[0])
+    kc, kf = _quant(seed, "k", B, H, Nkv, d, descales[1])
+    vc, vf = _quant(seed, "v", B, H, Nkv, d, descales[2])
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward_fp8(*(torch.from_numpy(c).cuda() for c in (qc, kc, vc)), *descales, scale=scale,
+                            causal=causal)
+    fa.device_status()
+    heads = [(b, h) for b in range(B) for h in range(H)] if sample is None else sample[0]
+    for b, h in heads:
+        rows = None if sample is None else sample[1]
+        ro, rl = oracle.attention_rows(qf[b, h], kf[b, h], vf[b, h], scale,
+                                       np.arange(Nq) if rows is None else rows, causal=causal)
+        got = cpu64(o[b, h]) if rows is None else cpu64(o[b, h])[rows]
+        gl = cpu64(lse[b, h]) if rows is None else cpu64(lse[b, h])[rows]
+        bnd = _bound(qf[b, h], kf[b, h], vf[b, h], scale, causal, rows)
+        assert np.all(np.abs(got - ro) <= bnd), (b, h, float(np.max(np.abs(got - ro) - bnd)))
+        assert np.max(np.abs(gl - rl)) <= 1e-3, (b, h)
+    return o
+
+
+@pytest.mark.parametrize("B,H,Nq,Nkv", [(1, 2, 256, 256), (2, 2, 300, 577), (1, 1, 129, 129)])
+def test_fp8_forward_within_derived_bound(B, H, Nq, Nkv):
+    _check(51, B, H, Nq, Nkv)
+
+
+def test_fp8_forward_with_descale_factors():
+    _check(52, 1, 2, 256, 512, descales=(0.25, 2.0, 0.5))
+
+
+def test_fp8_forward_causal():
+    _check(53, 1, 2, 384, 384, causal=True)
+
+
+def test_fp8_relative_error_matches_the_rounding_rms_on_spread_attention():
+    """With N(0,1) inputs attention is spread over many keys, so O's relative
+    error follows the RMS relative error of rounding P̃ to E4M3: for a 3-bit
+    mantissa at most 2^-4/√3 ≈ 0.036 (about 0.026 averaged over mantissas)."""
+    import torch
+    B, H, N, d = 1, 2, 1024, 128
+    qc, qf = _quant(54, "q", B, H, N, d, 1.0)
+    kc, kf = _quant(54, "k", B, H, N, d, 1.0)
+    vc, vf = _quant(54, "v", B, H, N, d, 1.0)
+    o, _ = fa.forward_fp8(*(torch.from_numpy(c).cuda() for c in (qc, kc, vc)))
+    ro, _ = oracle.attention_forward(qf, kf, vf, 1 / math.sqrt(d))
+    rel = np.linalg.norm(cpu64(o) - ro) / np.linalg.norm(ro)
+    assert rel <= 2.0 ** -4 / math.sqrt(3), rel
+
+
+@pytest.mark.slow
+def test_fp8_prefill_full_size_sampled():
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([[0, 255, 256, 4095], np.sort(rng.choice(4096, 40, replace=False))])
+    _check(55, 4, 32, 4096, 4096, sample=([(0, 0), (3, 31), (2, 5)], rows))

@@ -40,3 +40,18 @@ def test_bf16_rounding_matches_torch():
 def test_distribution_is_standard_normal():
     x = inputs.normal_slice(0, "q", 0, 0, 4096, 64)
     assert abs(float(x.mean())) < 0.01 and abs(float(x.std()) - 1.0) < 0.01
+
+
+def test_e4m3_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8")
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(200000).astype(np.float32) * s for s in (1.0, 0.01, 30.0)] +
+                       [np.array([0.0, -0.0, 448.0, 460.0, 1e6, -1e6, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10,
+                                  0.0625, 0.06640625, 1.0625, 1.1875], dtype=np.float32)])
+    ours = inputs.f32_to_e4m3_bits(x)
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    back = inputs.e4m3_bits_to_f32(ours)
+    assert np.array_equal(back, torch.from_numpy(ref).view(torch.float8_e4m3fn).float().numpy())
