@@ -412,6 +412,328 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 forward with P̃ kept in tensor memory.
+//
+// The same per-tile arithmetic as above, but P̃_i is written as bf16 pairs into
+// TMEM over the columns of S_i and the update O_i += P̃_i V_j reads it from
+// there (A operand in TMEM, V from shared memory).  That removes P̃'s shared-
+// memory round trip — the stores, the async-proxy fence and half of the PV
+// operand reads — which matters because an M = N = 128 shared-memory MMA
+// already consumes the tensor cores' whole shared-memory read path.
+// Since S_i(j+1) overwrites P̃_i(j), the MMA warp issues it right after
+// P̃_i(j)V_j (the tensor pipe runs a thread's MMAs in order), and the two query
+// tiles alternate:  … P̃_0(j)V_j, S_0(j+1), P̃_1(j)V_j, S_1(j+1), P̃_0(j+1)V_{j+1} …
+// so each softmax warpgroup's exponentials overlap the other tile's MMAs.
+// One commit per query tile and key tile: s_full[i] says S_i(j) is ready and,
+// because it follows P̃_i(j−1)V_{j−1}, that O_i is stable (for the rescale) and
+// V_{j−1}, K_j have been read by both tiles once i = 1 (a softmax thread of tile
+// 1 then hands those ring slots back to the producer).  K and V load in natural
+// order K_0, V_0, K_1, V_1, … through a deeper ring (no P̃ tiles in shared memory).
+template <int D>
+struct TsLayout {
+  static constexpr int kNKB = D / 64;              // 128-byte blocks along the head dim
+  static constexpr int kSlot = kNKB * kTileBytes;  // one Q, K or V tile
+  static constexpr int kRing = D == 128 ? 5 : 8;
+  static constexpr int kQ = 0;
+  static constexpr int kR = kQ + kQT * kSlot;
+  static constexpr int kBar = kR + kRing * kSlot;
+  static constexpr int kUsed = kBar + 512;
+  static constexpr int kSmem = (kUsed + 1024) < 120 * 1024 ? 120 * 1024 : (kUsed + 1024);
+};
+
+struct TsBars {
+  uint64_t q_full;
+  uint64_t r_full[8], r_empty[8];
+  uint64_t s_full[kQT];  // S_i(j) in TMEM; after the last key tile: O_i complete
+  uint64_t p_full[kQT];  // P̃_i(j) in TMEM (and O_i rescaled if needed)
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_constant__ FwdParams p) {
+  using L = TsLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  TsBars* bars = reinterpret_cast<TsBars*>(smem + L::kBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int mt = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int m0 = mt * (kQT * kBM);
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int off = p.Nkv - p.Nq;  // >= 0 whenever causal
+  const int kv_end = p.causal ? min(p.Nkv, m0 + kQT * kBM + off) : p.Nkv;
+  const int T = (kv_end + kBN - 1) / kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < L::kRing; ++s) {
+      mbar_init(&bars->r_full[s], 1);
+      mbar_init(&bars->r_empty[s], 1);
+    }
+    for (int i = 0; i < kQT; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 128);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(&bars->q_full, kQT * L::kSlot);
+      for (int i = 0; i < kQT; ++i)
+        for (int kb = 0; kb < L::kNKB; ++kb)
+          tma_load_4d(smem + L::kQ + i * L::kSlot + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64,
+                      m0 + i * kBM, h, b);
+      // Load t is K_{t/2} (t even) or V_{t/2} (t odd), into slot t % kRing.
+      int issued = 0;
+      for (int t = 0; t < 2 * T; ++t) {
+        const int slot = t % L::kRing;
+        const uint32_t u = t / L::kRing;
+        if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        mbar_arrive_expect_tx(&bars->r_full[slot], L::kSlot);
+        const CUtensorMap* tm = (t & 1) ? &p.tm_v : &p.tm_k;
+        for (int kb = 0; kb < L::kNKB; ++kb)
+          tma_load_4d(smem + L::kR + slot * L::kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
+                      (t >> 1) * kBN, h, b);
+        ++issued;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(&bars->q_full, 0, 200000000ull);
+        for (int t = (issued > L::kRing ? issued - L::kRing : 0); t < issued; ++t)
+          mbar_wait_drain(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
+      const uint32_t sQ = smem_u32(smem + L::kQ);
+      const uint32_t sR = smem_u32(smem + L::kR);
+      auto ring_wait = [&](int t, unsigned int where) -> bool {
+        return mbar_wait(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, abort_flag, p.err, site(where));
+      };
+      auto issue_s = [&](int i, uint32_t kb) {  // S_i = Q_i K_jᵀ
+        const uint32_t qb = sQ + i * L::kSlot;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + i * kBN, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), kIdescS,
+                      kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, site(5)) && ring_wait(0, 6);
+      if (ok) {
+        tc_fence_after();
+        for (int i = 0; i < kQT; ++i) {
+          issue_s(i, sR);
+          mma_commit(&bars->s_full[i]);
+        }
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const int tv = 2 * j + 1;
+        if (!(ok = ring_wait(tv, 3))) break;
+        const uint32_t vb = sR + (tv % L::kRing) * L::kSlot;
+        const bool next = j + 1 < T;
+        const uint32_t kb = sR + ((tv + 1) % L::kRing) * L::kSlot;
+        for (int i = 0; i < kQT && ok; ++i) {
+          if (!(ok = mbar_wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
+          if (i == 0 && next && !(ok = ring_wait(tv + 1, 6))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)  // O_i += P̃_i V_j, P̃_i (bf16 pairs) in S_i's columns
+            mma_bf16_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8,
+                        sdesc_sw128(vb + kk * 2048, kTileBytes, 1024), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          if (next) issue_s(i, kb);
+          mma_commit(&bars->s_full[i]);
+        }
+      }
+      if (*abort_flag) {
+        mma_commit(&bars->drain);
+        mbar_wait_drain(&bars->drain, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------- softmax / epilogue
+    const int qt = (warp - 2) >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_col = qt * kBN;
+    const uint32_t o_col = kColO + qt * 128;
+    const float sl2 = p.scale_log2;
+    const bool releaser = qt == kQT - 1 && wq == 0 && lane == 0;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      ok = mbar_wait(&bars->s_full[qt], j & 1, abort_flag, p.err, site(8));
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // S_1(j) is complete, so K_j and V_{j−1} have been read by both tiles.
+      if (releaser) {
+        mbar_arrive(&bars->r_empty[(2 * j) % L::kRing]);
+        if (j >= 1) mbar_arrive(&bars->r_empty[(2 * j - 1) % L::kRing]);
+      }
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        const uint32_t sa = tmem + lane_base + s_col;
+        tmem_ld32(sa + 0, r0);
+        tmem_ld32(sa + 32, r1);
+        tmem_ld32(sa + 64, r2);
+        tmem_ld32(sa + 96, r3);
+        tmem_wait_ld();
+        reg_fence(r0);
+        reg_fence(r1);
+        reg_fence(r2);
+        reg_fence(r3);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(r0[c]);
+          s[32 + c] = __uint_as_float(r1[c]);
+          s[64 + c] = __uint_as_float(r2[c]);
+          s[96 + c] = __uint_as_float(r3[c]);
+        }
+      }
+      int kv_valid = p.Nkv - j * kBN;
+      if (p.causal) kv_valid = min(kv_valid, m0 + qt * kBM + row + off + 1 - j * kBN);
+      if (kv_valid < kBN) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= kv_valid) s[c] = -INFINITY;
+      }
+      // Row max: four independent chains of three-input maxima.
+      float mx4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx4[i] = fmax3(s[i], s[4 + i], s[8 + i]);
+#pragma unroll
+      for (int c = 12; c < 124; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], s[c + i], s[c + 4 + i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx4[i] = fmaxf(mx4[i], s[124 + i]);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float m_cand = fmaxf(m_run, mx * sl2);
+      const bool need = m_cand > m_run + kRescaleLog2;  // always true while m_run = −∞
+      const float m_new = need ? m_cand : m_run;
+      const float corr = need ? ex2_approx(m_run - m_new) : 1.f;
+      float rs[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+      const float nm = -m_new;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        // P̃ for keys 64·hf … 64·hf+63, then 32 columns of bf16 pairs into TMEM.
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 64 * hf; c < 64 * hf + 64; c += 8) {
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            float x0, x1;
+            ffma2(x0, x1, s[c + i], s[c + i + 1], sl2, sl2, nm, nm);
+            x0 = ex2_approx(x0);
+            x1 = ex2_approx(x1);
+            fadd2(rs[i], rs[i + 1], rs[i], rs[i + 1], x0, x1);
+            w[(c + i - 64 * hf) >> 1] = pack_bf16x2(x0, x1);
+          }
+        }
+        tmem_st32(tmem + lane_base + s_col + 32 * hf, w);
+      }
+      const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+      l_run = l_run * corr + rsum;
+      // O_i is stable here (its last update came before S_i(j)); rescale it in
+      // TMEM only when some row of this warp moved its reference max.
+      if (j >= 1 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          const uint32_t oa = tmem + lane_base + o_col + c * 32;
+          tmem_ld32(oa, r);
+          tmem_wait_ld();
+          reg_fence(r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+          tmem_st32(oa, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[qt]);
+      m_run = m_new;
+    }
+    if (ok) {
+      ok = mbar_wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const float inv = p.o_scale / l_run;
+        const int grow = m0 + qt * kBM + row;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + b * p.o_sb + h * p.o_sh +
+                              static_cast<int64_t>(grow) * p.o_sn;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + o_col + c * 32, r);
+          tmem_wait_ld();
+          reg_fence(r);
+          if (grow < p.Nq) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * inv, __uint_as_float(r[8 * q4 + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * inv, __uint_as_float(r[8 * q4 + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * inv, __uint_as_float(r[8 * q4 + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * inv, __uint_as_float(r[8 * q4 + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = v;
+            }
+          }
+        }
+        if (p.lse != nullptr && grow < p.Nq)
+          p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + grow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_ts(const FwdParams& p, cudaStream_t stream) {
+  using L = TsLayout<D>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_ts_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.Nq + kQT * kBM - 1) / (kQT * kBM), p.H, p.B);
+  fwd_ts_kernel<D><<<grid, kThreads, L::kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D, bool FP8>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<D, FP8>;
@@ -426,8 +748,8 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch_impl<128, false>(p, stream);
-  if (d == 64) return launch_impl<64, false>(p, stream);
+  if (d == 128) return launch_ts<128>(p, stream);
+  if (d == 64) return launch_ts<64>(p, stream);
   return cudaErrorInvalidValue;
 }
 
