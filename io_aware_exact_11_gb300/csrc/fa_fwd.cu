@@ -1,4 +1,5 @@
-// fa_fwd.cu — forward attention on tcgen05 tensor cores (bf16 in, fp32 accumulate).
+// fa_fwd.cu — forward attention on tcgen05 tensor cores (bf16 or E4M3 in,
+// fp32 accumulate).
 //
 // One CTA owns two 128-row query tiles Q_0, Q_1 (256 consecutive rows) of one
 // (b, h) and streams every key/value tile K_j, V_j (128 keys) past both, as in
@@ -12,20 +13,30 @@
 // and after the last tile O_i/ℓ and LSE = m + ln ℓ are written once.
 // Exponentials run in base 2 with σ·log2(e) folded into the scores.
 //
+// P̃ never leaves the SM's tensor memory: the softmax warps write it (bf16
+// pairs, or four E4M3 codes, per 32-bit column) over the columns of S_i, and
+// O_i += P̃_i V_j takes it from there as its A operand (V from shared memory).
+// An M = N = 128 MMA with both operands in shared memory already uses the tensor
+// cores' whole shared-memory read path, so a P̃ round trip through shared
+// memory would cost tensor throughput.  Because S_i(j+1) overwrites P̃_i(j), the
+// MMA warp issues it right after P̃_i(j)V_j (a thread's tcgen05 MMAs execute in
+// order), and the two query tiles alternate:
+//   … P̃_0(j)V_j, S_0(j+1), P̃_1(j)V_j, S_1(j+1), P̃_0(j+1)V_{j+1} …
+// so each softmax warpgroup's exponentials overlap the other tile's MMAs.
+// One tcgen05.commit per query tile and key tile: s_full[i] says S_i(j) is in
+// TMEM and, because it follows P̃_i(j−1)V_{j−1}, that O_i is stable for a
+// rescale; once S_1(j) is complete both tiles have read K_j and V_{j−1}, so a
+// softmax thread of tile 1 hands those ring slots back to the producer.
+//
 // Warp roles (320 threads):
-//   warp 0       TMA producer: Q_0, Q_1 once, then K_0, K_1, V_0, K_2, V_1, …
-//                (keys run one tile ahead) into a 3-slot shared-memory ring
-//   warp 1       TMEM owner and MMA issuer (one thread); per key tile it issues
-//                S_0(j), S_1(j), then P̃_0(j−1)V_{j−1}, P̃_1(j−1)V_{j−1}
+//   warp 0       TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, … through
+//                a shared-memory ring (5 slots at d = 128 bf16)
+//   warp 1       TMEM owner and MMA issuer (one thread)
 //   warps 2..5   softmax / rescale / epilogue of Q_0 (warp w reads TMEM lanes 32·(w%4)…)
 //   warps 6..9   the same for Q_1
-// Two softmax warpgroups put two independent softmax warps on every SM
-// sub-partition, so one's exponentials and TMEM loads overlap the other's, and
-// the tensor cores always have the other tile's MMAs queued.  Sharing each
-// K/V tile between two query tiles also halves the L2 → SM traffic.
-// TMEM: S_0 (columns 0..127), S_1 (128..255), O_0 (256..), O_1 (384..).
-// Shared memory holds every operand in the 128-byte-swizzled layout TMA writes:
-// blocks of [128 rows][64 bf16]; P̃_i is written there by its softmax warps.
+// TMEM: S_0 / P̃_0 (columns 0..127), S_1 / P̃_1 (128..255), O_0 (256..), O_1 (384..).
+// Shared memory holds Q, K, V in the 128-byte-swizzled layout TMA writes:
+// blocks of [128 rows][128 bytes].
 //
 // Causal mask (the lesson's §5 lab uses is_causal=True), bottom-right aligned:
 // row i sees keys j <= i + (N_kv − N_q).  A CTA streams only the key tiles its
@@ -35,7 +46,7 @@
 // FP8 (E4M3) variant, FlashAttention-3's addition noted in the lesson (§3.3) and
 // the interview notes (§四.5): Q, K, V arrive as E4M3 with per-tensor descale
 // factors, the MMAs run as kind::f8f6f4 (32 elements per instruction, still 32
-// bytes per k-step), P̃ is written as E4M3 (lazy rescaling keeps it <= 256, inside
+// bytes per k-step), P̃ is stored as E4M3 (lazy rescaling keeps it <= 256, inside
 // E4M3's ±448) and ℓ sums the unrounded fp32 values; O leaves as bf16.
 //
 // Lazy rescaling: a row keeps its reference max m until a tile's max exceeds
@@ -54,7 +65,7 @@ namespace {
 constexpr int kBM = 128;          // rows per query tile
 constexpr int kQT = 2;            // query tiles per CTA
 constexpr int kBN = 128;          // keys per key/value tile
-constexpr int kTileBytes = 128 * 128;  // one [128 rows][64 bf16] swizzled block
+constexpr int kTileBytes = 128 * 128;  // one [128 rows][128 bytes] swizzled block
 constexpr int kThreads = 64 + kQT * 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
@@ -65,13 +76,11 @@ struct FwdLayout {
   static constexpr int kEB = FP8 ? 1 : 2;            // bytes per element
   static constexpr int kNKB = D * kEB / 128;         // 128-byte blocks along the head dim
   static constexpr int kSlot = kNKB * kTileBytes;    // one Q, K or V tile
-  static constexpr int kPB = kBN * kEB / 128;        // 128-byte blocks of one P̃ row
   static constexpr int kStepK = 32 / kEB;            // elements per MMA k-step (32 bytes)
-  static constexpr int kRing = 3;                   // K_j, V_j, K_{j+1} in flight
+  static constexpr int kRing = kSlot >= 32768 ? 5 : 8;
   static constexpr int kQ = 0;
   static constexpr int kR = kQ + kQT * kSlot;
-  static constexpr int kP = kR + kRing * kSlot;     // one P̃ tile per query tile
-  static constexpr int kBar = kP + kQT * kPB * kTileBytes;
+  static constexpr int kBar = kR + kRing * kSlot;
   static constexpr int kUsed = kBar + 512;
   // +1 KB so the base can be rounded up to 1024; at least 120 KB so only one
   // CTA (which owns all 512 TMEM columns) is resident per SM.
@@ -80,9 +89,9 @@ struct FwdLayout {
 
 struct FwdBars {
   uint64_t q_full;
-  uint64_t r_full[3], r_empty[3];
-  uint64_t s_full[kQT], s_free[kQT];
-  uint64_t p_full[kQT], p_free[kQT];  // p_free[i]: the P̃_i V MMA has finished
+  uint64_t r_full[8], r_empty[8];
+  uint64_t s_full[kQT];  // S_i(j) in TMEM; after the last key tile: O_i complete
+  uint64_t p_full[kQT];  // P̃_i(j) in TMEM (and O_i rescaled if needed)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -98,14 +107,8 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// Position in the load sequence K_0, K_1, V_0, K_2, V_1, K_3, …, V_{T−1}: keys run
-// one tile ahead of values, which is also the order the MMA warp consumes them
-// (S(j) needs K_j; P̃(j−1)V_{j−1} is issued right after it).
-__device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
-__device__ __forceinline__ int seq_v(int j, int T) { return min(2 * j + 2, 2 * T - 1); }
-
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -131,354 +134,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     }
     for (int i = 0; i < kQT; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 128);
-      mbar_init(&bars->p_full[i], 128);
-      mbar_init(&bars->p_free[i], 1);
-    }
-    mbar_init(&bars->drain, 1);
-    bars->abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, kQT * L::kSlot);
-      for (int i = 0; i < kQT; ++i)
-        for (int kb = 0; kb < L::kNKB; ++kb)
-          tma_load_4d(smem + L::kQ + i * L::kSlot + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64,
-                      m0 + i * kBM, h, b);
-      // Load t (sequence K_0, K_1, V_0, K_2, V_1, …, V_{T−1}) goes to slot t % 3.
-      int issued = 0;
-      for (int t = 0; t < 2 * T; ++t) {
-        const int slot = t % L::kRing;
-        const uint32_t u = t / L::kRing;
-        bool is_v;
-        int jt;
-        if (t == 0) { is_v = false; jt = 0; }
-        else if (t == 2 * T - 1) { is_v = true; jt = T - 1; }
-        else if (t & 1) { is_v = false; jt = (t + 1) >> 1; }
-        else { is_v = true; jt = (t - 2) >> 1; }
-        if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
-        mbar_arrive_expect_tx(&bars->r_full[slot], L::kSlot);
-        const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
-        for (int kb = 0; kb < L::kNKB; ++kb)
-          tma_load_4d(smem + L::kR + slot * L::kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
-                      jt * kBN, h, b);
-        ++issued;
-      }
-      if (*abort_flag) {
-        // Let every copy this thread started land before the CTA exits.
-        mbar_wait_drain(&bars->q_full, 0, 200000000ull);
-        for (int t = (issued > L::kRing ? issued - L::kRing : 0); t < issued; ++t)
-          mbar_wait_drain(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, 200000000ull);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t kIdescO = FP8 ? idesc_e4m3_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
-      auto mma = [&](uint32_t dst, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
-        if (FP8)
-          mma_e4m3_ss(dst, ad, bd, id, acc);
-        else
-          mma_bf16_ss(dst, ad, bd, id, acc);
-      };
-      const uint32_t sQ = smem_u32(smem + L::kQ);
-      const uint32_t sR = smem_u32(smem + L::kR);
-      const uint32_t sP = smem_u32(smem + L::kP);
-      auto issue_pv = [&](int jj) -> bool {
-        const int t = seq_v(jj, T);
-        const int slot = t % L::kRing;
-        if (!mbar_wait(&bars->r_full[slot], (t / L::kRing) & 1, abort_flag, p.err, site(3))) return false;
-        const uint32_t vb = sR + slot * L::kSlot;
-        for (int i = 0; i < kQT; ++i) {
-          if (!mbar_wait(&bars->p_full[i], jj & 1, abort_flag, p.err, site(4))) return false;
-          tc_fence_after();
-          const uint32_t pbuf = sP + i * L::kPB * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kBN / L::kStepK; ++kk) {
-            // A = P̃_i (K-major, keys along K); B = V_j (MN-major: head dim contiguous).
-            const uint64_t ad = sdesc_sw128(pbuf + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(vb + kk * L::kStepK * 128, kTileBytes, 1024);
-            mma(tmem + kColO + i * 128, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars->p_free[i]);
-        }
-        mma_commit(&bars->r_empty[slot]);
-        return true;
-      };
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, site(5));
-      for (int j = 0; ok && j < T; ++j) {
-        const int t = seq_k(j);
-        const int slot = t % L::kRing;
-        if (!(ok = mbar_wait(&bars->r_full[slot], (t / L::kRing) & 1, abort_flag, p.err, site(6)))) break;
-        const uint32_t kb = sR + slot * L::kSlot;
-        for (int i = 0; i < kQT && ok; ++i) {
-          if (!(ok = mbar_wait(&bars->s_free[i], (j & 1) ^ 1, abort_flag, p.err, site(7)))) break;
-          tc_fence_after();
-          const uint32_t qb = sQ + i * L::kSlot;
-#pragma unroll
-          for (int kk = 0; kk < D / L::kStepK; ++kk) {
-            const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-            mma(tmem + i * kBN, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescS,
-                kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->s_full[i]);
-        }
-        if (!ok) break;
-        mma_commit(&bars->r_empty[slot]);
-        if (j >= 1) ok = issue_pv(j - 1);
-      }
-      if (ok) issue_pv(T - 1);
-      if (*abort_flag) {
-        mma_commit(&bars->drain);
-        mbar_wait_drain(&bars->drain, 0, 200000000ull);
-      }
-    }
-  } else {
-    // ------------------------------------------------- softmax / epilogue
-    const int qt = (warp - 2) >> 2;          // which query tile
-    const int wq = warp & 3;                 // TMEM lane quarter
-    const int row = wq * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_col = qt * kBN;
-    const uint32_t o_col = kColO + qt * 128;
-    const float sl2 = p.scale_log2;
-    uint8_t* pbuf = smem + L::kP + qt * L::kPB * kTileBytes;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(&bars->s_full[qt], j & 1, abort_flag, p.err, site(8));
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      const uint32_t sa = tmem + lane_base + s_col;
-      tmem_ld32(sa + 0, r0);
-      tmem_ld32(sa + 32, r1);
-      tmem_ld32(sa + 64, r2);
-      tmem_ld32(sa + 96, r3);
-      tmem_wait_ld();
-      reg_fence(r0);
-      reg_fence(r1);
-      reg_fence(r2);
-      reg_fence(r3);
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[qt]);
-
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = __uint_as_float(r0[c]);
-        s[32 + c] = __uint_as_float(r1[c]);
-        s[64 + c] = __uint_as_float(r2[c]);
-        s[96 + c] = __uint_as_float(r3[c]);
-      }
-      int kv_valid = p.Nkv - j * kBN;
-      if (p.causal) kv_valid = min(kv_valid, m0 + qt * kBM + row + off + 1 - j * kBN);
-      if (kv_valid < kBN) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= kv_valid) s[c] = -INFINITY;
-      }
-      // Row max with eight independent chains.
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < 128; c += 8) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_cand = fmaxf(m_run, mx * sl2);
-      const bool need = m_cand > m_run + kRescaleLog2;   // always true while m_run = −∞
-      const float m_new = need ? m_cand : m_run;
-      const float corr = need ? ex2_approx(m_run - m_new) : 1.f;
-      float rs8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          s[c + i] = ex2_approx(fmaf(s[c + i], sl2, -m_new));
-          rs8[i] += s[c + i];
-        }
-      }
-      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-      l_run = l_run * corr + rs;
-
-      // P̃_i and O_i are free once the P̃_i V MMA of tile j−1 has finished.
-      ok = mbar_wait(&bars->p_free[qt], (j & 1) ^ 1, abort_flag, p.err, site(9));
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      if (FP8) {
-        // 16 keys per 16-byte chunk, one 128-byte block per row.
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 v;
-          v.x = pack_e4m3x4(s[16 * cc + 0], s[16 * cc + 1], s[16 * cc + 2], s[16 * cc + 3]);
-          v.y = pack_e4m3x4(s[16 * cc + 4], s[16 * cc + 5], s[16 * cc + 6], s[16 * cc + 7]);
-          v.z = pack_e4m3x4(s[16 * cc + 8], s[16 * cc + 9], s[16 * cc + 10], s[16 * cc + 11]);
-          v.w = pack_e4m3x4(s[16 * cc + 12], s[16 * cc + 13], s[16 * cc + 14], s[16 * cc + 15]);
-          *reinterpret_cast<uint4*>(pbuf + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
-        }
-      } else {
-#pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
-          uint4 v;
-          v.x = pack_bf16x2(s[8 * c8 + 0], s[8 * c8 + 1]);
-          v.y = pack_bf16x2(s[8 * c8 + 2], s[8 * c8 + 3]);
-          v.z = pack_bf16x2(s[8 * c8 + 4], s[8 * c8 + 5]);
-          v.w = pack_bf16x2(s[8 * c8 + 6], s[8 * c8 + 7]);
-          const int kb = c8 >> 3;
-          const int cc = c8 & 7;
-          *reinterpret_cast<uint4*>(pbuf + kb * kTileBytes + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
-        }
-      }
-      // Rescale the running output only when some row of this warp moved its
-      // reference max.
-      if (j >= 1 && __any_sync(0xffffffffu, need)) {
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          const uint32_t oa = tmem + lane_base + o_col + c * 32;
-          tmem_ld32(oa, r);
-          tmem_wait_ld();
-          reg_fence(r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-          tmem_st32(oa, r);
-        }
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[qt]);
-      m_run = m_new;
-    }
-    if (ok) {
-      ok = mbar_wait(&bars->p_free[qt], (T - 1) & 1, abort_flag, p.err, site(10));
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        const float inv = p.o_scale / l_run;
-        const int grow = m0 + qt * kBM + row;
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + b * p.o_sb + h * p.o_sh +
-                              static_cast<int64_t>(grow) * p.o_sn;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + o_col + c * 32, r);
-          tmem_wait_ld();
-          reg_fence(r);
-          if (grow < p.Nq) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * inv, __uint_as_float(r[8 * q4 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * inv, __uint_as_float(r[8 * q4 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * inv, __uint_as_float(r[8 * q4 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * inv, __uint_as_float(r[8 * q4 + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = v;
-            }
-          }
-        }
-        if (p.lse != nullptr && grow < p.Nq)
-          p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + grow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// bf16 forward with P̃ kept in tensor memory.
-//
-// The same per-tile arithmetic as above, but P̃_i is written as bf16 pairs into
-// TMEM over the columns of S_i and the update O_i += P̃_i V_j reads it from
-// there (A operand in TMEM, V from shared memory).  That removes P̃'s shared-
-// memory round trip — the stores, the async-proxy fence and half of the PV
-// operand reads — which matters because an M = N = 128 shared-memory MMA
-// already consumes the tensor cores' whole shared-memory read path.
-// Since S_i(j+1) overwrites P̃_i(j), the MMA warp issues it right after
-// P̃_i(j)V_j (the tensor pipe runs a thread's MMAs in order), and the two query
-// tiles alternate:  … P̃_0(j)V_j, S_0(j+1), P̃_1(j)V_j, S_1(j+1), P̃_0(j+1)V_{j+1} …
-// so each softmax warpgroup's exponentials overlap the other tile's MMAs.
-// One commit per query tile and key tile: s_full[i] says S_i(j) is ready and,
-// because it follows P̃_i(j−1)V_{j−1}, that O_i is stable (for the rescale) and
-// V_{j−1}, K_j have been read by both tiles once i = 1 (a softmax thread of tile
-// 1 then hands those ring slots back to the producer).  K and V load in natural
-// order K_0, V_0, K_1, V_1, … through a deeper ring (no P̃ tiles in shared memory).
-template <int D>
-struct TsLayout {
-  static constexpr int kNKB = D / 64;              // 128-byte blocks along the head dim
-  static constexpr int kSlot = kNKB * kTileBytes;  // one Q, K or V tile
-  static constexpr int kRing = D == 128 ? 5 : 8;
-  static constexpr int kQ = 0;
-  static constexpr int kR = kQ + kQT * kSlot;
-  static constexpr int kBar = kR + kRing * kSlot;
-  static constexpr int kUsed = kBar + 512;
-  static constexpr int kSmem = (kUsed + 1024) < 120 * 1024 ? 120 * 1024 : (kUsed + 1024);
-};
-
-struct TsBars {
-  uint64_t q_full;
-  uint64_t r_full[8], r_empty[8];
-  uint64_t s_full[kQT];  // S_i(j) in TMEM; after the last key tile: O_i complete
-  uint64_t p_full[kQT];  // P̃_i(j) in TMEM (and O_i rescaled if needed)
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_constant__ FwdParams p) {
-  using L = TsLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  uint8_t* smem = smem_raw + pad;
-  TsBars* bars = reinterpret_cast<TsBars*>(smem + L::kBar);
-  volatile int* abort_flag = &bars->abort_flag;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int mt = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int m0 = mt * (kQT * kBM);
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int off = p.Nkv - p.Nq;  // >= 0 whenever causal
-  const int kv_end = p.causal ? min(p.Nkv, m0 + kQT * kBM + off) : p.Nkv;
-  const int T = (kv_end + kBN - 1) / kBN;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < L::kRing; ++s) {
-      mbar_init(&bars->r_full[s], 1);
-      mbar_init(&bars->r_empty[s], 1);
-    }
-    for (int i = 0; i < kQT; ++i) {
-      mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 128);
     }
     mbar_init(&bars->drain, 1);
@@ -503,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_consta
       mbar_arrive_expect_tx(&bars->q_full, kQT * L::kSlot);
       for (int i = 0; i < kQT; ++i)
         for (int kb = 0; kb < L::kNKB; ++kb)
-          tma_load_4d(smem + L::kQ + i * L::kSlot + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64,
+          tma_load_4d(smem + L::kQ + i * L::kSlot + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * (128 / L::kEB),
                       m0 + i * kBM, h, b);
       // Load t is K_{t/2} (t even) or V_{t/2} (t odd), into slot t % kRing.
       int issued = 0;
@@ -514,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_consta
         mbar_arrive_expect_tx(&bars->r_full[slot], L::kSlot);
         const CUtensorMap* tm = (t & 1) ? &p.tm_v : &p.tm_k;
         for (int kb = 0; kb < L::kNKB; ++kb)
-          tma_load_4d(smem + L::kR + slot * L::kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
-                      (t >> 1) * kBN, h, b);
+          tma_load_4d(smem + L::kR + slot * L::kSlot + kb * kTileBytes, tm, &bars->r_full[slot],
+                      kb * (128 / L::kEB), (t >> 1) * kBN, h, b);
         ++issued;
       }
       if (*abort_flag) {
@@ -527,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
+      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t kIdescO = FP8 ? idesc_e4m3_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
       const uint32_t sQ = smem_u32(smem + L::kQ);
       const uint32_t sR = smem_u32(smem + L::kR);
       auto ring_wait = [&](int t, unsigned int where) -> bool {
@@ -537,10 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_consta
       auto issue_s = [&](int i, uint32_t kb) {  // S_i = Q_i K_jᵀ
         const uint32_t qb = sQ + i * L::kSlot;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / L::kStepK; ++kk) {
           const uint32_t o = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + i * kBN, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), kIdescS,
-                      kk > 0 ? 1u : 0u);
+          const uint64_t ad = sdesc_sw128(qb + o, 16, 1024), bd = sdesc_sw128(kb + o, 16, 1024);
+          if (FP8)
+            mma_e4m3_ss(tmem + i * kBN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+          else
+            mma_bf16_ss(tmem + i * kBN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, site(5)) && ring_wait(0, 6);
@@ -561,10 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_consta
           if (!(ok = mbar_wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
           if (i == 0 && next && !(ok = ring_wait(tv + 1, 6))) break;
           tc_fence_after();
+          // O_i += P̃_i V_j: A = P̃_i from S_i's TMEM columns (32 bytes of keys = 8
+          // columns per k-step), B = V_j read MN-major (head dim contiguous).
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)  // O_i += P̃_i V_j, P̃_i (bf16 pairs) in S_i's columns
-            mma_bf16_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8,
-                        sdesc_sw128(vb + kk * 2048, kTileBytes, 1024), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / L::kStepK; ++kk) {
+            const uint64_t bd = sdesc_sw128(vb + kk * L::kStepK * 128, kTileBytes, 1024);
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            if (FP8)
+              mma_e4m3_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
+            else
+              mma_bf16_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
+          }
           if (next) issue_s(i, kb);
           mma_commit(&bars->s_full[i]);
         }
@@ -646,21 +311,32 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_consta
       const float nm = -m_new;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        // P̃ for keys 64·hf … 64·hf+63, then 32 columns of bf16 pairs into TMEM.
+        // P̃ for keys 64·hf … 64·hf+63 into TMEM: 32 columns of bf16 pairs, or
+        // 16 columns of four E4M3 codes (first key in the lowest bits).
         uint32_t w[32];
 #pragma unroll
         for (int c = 64 * hf; c < 64 * hf + 64; c += 8) {
+          float x[8];
 #pragma unroll
           for (int i = 0; i < 8; i += 2) {
-            float x0, x1;
-            ffma2(x0, x1, s[c + i], s[c + i + 1], sl2, sl2, nm, nm);
-            x0 = ex2_approx(x0);
-            x1 = ex2_approx(x1);
-            fadd2(rs[i], rs[i + 1], rs[i], rs[i + 1], x0, x1);
-            w[(c + i - 64 * hf) >> 1] = pack_bf16x2(x0, x1);
+            ffma2(x[i], x[i + 1], s[c + i], s[c + i + 1], sl2, sl2, nm, nm);
+            x[i] = ex2_approx(x[i]);
+            x[i + 1] = ex2_approx(x[i + 1]);
+            fadd2(rs[i], rs[i + 1], rs[i], rs[i + 1], x[i], x[i + 1]);
+          }
+          const int wc = (c - 64 * hf) >> (FP8 ? 2 : 1);
+          if (FP8) {
+            w[wc] = pack_e4m3x4(x[0], x[1], x[2], x[3]);
+            w[wc + 1] = pack_e4m3x4(x[4], x[5], x[6], x[7]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[wc + i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
           }
         }
-        tmem_st32(tmem + lane_base + s_col + 32 * hf, w);
+        if (FP8)
+          tmem_st16(tmem + lane_base + s_col + 16 * hf, reinterpret_cast<uint32_t(&)[16]>(w));
+        else
+          tmem_st32(tmem + lane_base + s_col + 32 * hf, w);
       }
       const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       l_run = l_run * corr + rsum;
@@ -724,32 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_ts_kernel(const __grid_consta
   }
 }
 
-template <int D>
-cudaError_t launch_ts(const FwdParams& p, cudaStream_t stream) {
-  using L = TsLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_ts_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((p.Nq + kQT * kBM - 1) / (kQT * kBM), p.H, p.B);
-  fwd_ts_kernel<D><<<grid, kThreads, L::kSmem, stream>>>(p);
-  return cudaGetLastError();
-}
-
 template <int D, bool FP8>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<D, FP8>;
   cudaError_t e =
-      cudaFuncSetAttribute(fwd_bf16_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+      cudaFuncSetAttribute(fwd_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((p.Nq + kQT * kBM - 1) / (kQT * kBM), p.H, p.B);
-  fwd_bf16_kernel<D, FP8><<<grid, kThreads, L::kSmem, stream>>>(p);
+  fwd_kernel<D, FP8><<<grid, kThreads, L::kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch_ts<128>(p, stream);
-  if (d == 64) return launch_ts<64>(p, stream);
+  if (d == 128) return launch_impl<128, false>(p, stream);
+  if (d == 64) return launch_impl<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 
