@@ -52,6 +52,32 @@ def test_causal_forward_bf16(shape):
     _check(21, *shape, "bf16", TOL_O_BF16, TOL_LSE_BF16)
 
 
+@pytest.mark.parametrize("shape", [(2, 80, 700, 700, 128), (1, 160, 300, 1000, 128)])
+def test_causal_forward_many_items_per_cta(shape):
+    """More work items than SMs with unequal costs: the persistent CTAs take
+    items heaviest first (odd rounds reversed) and run several each.
+
+    The first causal rows average a handful of keys, so |O| comes close to
+    max|V| (about 5 over these 14M samples), where the bf16 output's own
+    rounding alone can exceed 1e-2.  Each element must therefore meet the fixed
+    1e-2 bound or, where bf16 forces more, the bound derived from the two bf16
+    roundings (8 significant bits, relative error <= 2^-8 each): P̃ entering
+    P̃·V gives at most 2^-8·(P|V|) and storing O at most 2^-8·|O|."""
+    B, H, Nq, Nkv, d = shape
+    host, dev = make_qkv(23, B, H, Nq, Nkv, d, "bf16")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale, causal=True)
+    fa.device_status()
+    q64, k64, v64 = (f64(host[n], "bf16") for n in ("q", "k", "v"))
+    ro, rl = oracle.attention_forward(q64, k64, v64, scale, causal=True)
+    pv = np.stack([np.stack([oracle.attention_probs(q64[b, h], k64[b, h], scale, causal=True) @ np.abs(v64[b, h])
+                             for h in range(H)]) for b in range(B)])
+    bound = np.maximum(TOL_O_BF16, 2.0 ** -8 * (pv + np.abs(ro)) + 1e-4)
+    err = np.abs(cpu64(o) - ro)
+    assert np.all(err <= bound), float(np.max(err - bound))
+    assert max_abs(cpu64(lse), rl) <= TOL_LSE_BF16
+
+
 @pytest.mark.parametrize("shape", [(1, 1, 256, 256, 64), (2, 2, 77, 100, 128)])
 def test_causal_forward_fp32(shape):
     _check(22, *shape, "fp32", TOL_FP32, TOL_FP32)

@@ -68,14 +68,28 @@ def test_forward_bf16_matches_oracle(shape):
     _fwd_check(1, B, H, Nq, Nkv, d, "bf16", TOL_O_BF16, TOL_LSE_BF16)
 
 
+@pytest.mark.parametrize("shape", [
+    (3, 70, 200, 300, 128),   # 210 work items: some CTAs run a second item; ragged rows and keys
+    (2, 100, 600, 130, 64),   # 600 items of two key tiles each, head dim 64
+    (4, 50, 256, 100, 128),   # 200 items of a single (ragged) key tile
+])
+def test_forward_bf16_many_items_per_cta(shape):
+    """More 256-row work items than SMs, so every persistent CTA runs several
+    items back to back: barrier phases, ring slots and the Q buffer carry over
+    from one item to the next."""
+    B, H, Nq, Nkv, d = shape
+    _fwd_check(3, B, H, Nq, Nkv, d, "bf16", TOL_O_BF16, TOL_LSE_BF16)
+
+
 def test_forward_bf16_large_scores():
     """Scores with standard deviation ~6 exercise the running-max rescale.
 
-    Bound derived from the arithmetic rather than the N(0,1) tolerance: the
-    probabilities enter P·V rounded to bf16 (relative error <= 2^-9, so at most
-    2^-9·max|V| in O) and O is stored as bf16 (<= 2^-9·|O|).  With peaked rows
-    |O| approaches max|V|, so the bound is 2^-8·max|V| plus fp32 noise.  LSE is
-    fp32 throughout: its error scales with its magnitude (~1e-6 relative).
+    Bound derived from the arithmetic rather than the N(0,1) tolerance.  bf16
+    keeps 8 significant bits, so one rounding has relative error <= 2^-8: the
+    probabilities enter P·V rounded to bf16 (at most 2^-8·max|V| in O) and O is
+    stored as bf16 (<= 2^-8·|O|).  With peaked rows |O| approaches max|V|, so the
+    bound is 2^-7·max|V| plus fp32 noise.  LSE is fp32 throughout: its error
+    scales with its magnitude (~1e-6 relative).
     """
     import torch
     B, H, N, d = 1, 2, 512, 128
@@ -84,7 +98,7 @@ def test_forward_bf16_large_scores():
     o, lse = fa.forward(q, dev["k"], dev["v"])
     v64 = f64(host["v"], "bf16")
     ref_o, ref_lse = oracle.attention_forward(cpu64(q), f64(host["k"], "bf16"), v64, 1 / math.sqrt(d))
-    assert max_abs(cpu64(o), ref_o) <= 2.0 ** -8 * float(np.abs(v64).max()) + 1e-3
+    assert max_abs(cpu64(o), ref_o) <= 2.0 ** -7 * float(np.abs(v64).max()) + 1e-3
     assert max_abs(cpu64(lse), ref_lse) <= TOL_LSE_BF16 * max(1.0, float(np.abs(ref_lse).max()) / 8)
 
 
