@@ -53,9 +53,9 @@ def test_causal_forward_bf16(shape):
 
 
 @pytest.mark.parametrize("shape", [(2, 80, 700, 700, 128), (1, 160, 300, 1000, 128)])
-def test_causal_forward_many_items_per_cta(shape):
-    """More work items than SMs with unequal costs: the persistent CTAs take
-    items heaviest first (odd rounds reversed) and run several each.
+def test_causal_forward_many_blocks(shape):
+    """More query blocks than SMs with unequal costs (the heaviest blocks are
+    scheduled first), over several waves.
 
     The first causal rows average a handful of keys, so |O| comes close to
     max|V| (about 5 over these 14M samples), where the bf16 output's own

@@ -83,8 +83,8 @@ def test_fp8_forward_within_derived_bound(B, H, Nq, Nkv):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_forward_many_items_per_cta(causal):
-    """320 work items, so each persistent CTA runs two or three of them."""
+def test_fp8_forward_many_blocks(causal):
+    """320 query blocks: more than the SMs, so the grid runs in several waves."""
     _check(54, 2, 80, 300, 300, causal=causal)
 
 

@@ -73,10 +73,9 @@ def test_forward_bf16_matches_oracle(shape):
     (2, 100, 600, 130, 64),   # 600 items of two key tiles each, head dim 64
     (4, 50, 256, 100, 128),   # 200 items of a single (ragged) key tile
 ])
-def test_forward_bf16_many_items_per_cta(shape):
-    """More 256-row work items than SMs, so every persistent CTA runs several
-    items back to back: barrier phases, ring slots and the Q buffer carry over
-    from one item to the next."""
+def test_forward_bf16_many_blocks(shape):
+    """More 256-row query blocks than SMs, so the grid runs in several waves
+    (and, for the 200-row case, every block has a ragged row tail)."""
     B, H, Nq, Nkv, d = shape
     _fwd_check(3, B, H, Nq, Nkv, d, "bf16", TOL_O_BF16, TOL_LSE_BF16)
 
