@@ -43,13 +43,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum), keyed by the sha256 of the kernel's sources at capture
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # profiles/fwd_bf16_kernel_prefill_B4_H32_N4096_d128.md
-    "fwd_prefill": {"src": "745faee6a3509062", "bytes": 402710272 + 117554944},
+    # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
+    "fwd_prefill": {"src": "c6c9bf8989b0aba3", "bytes": 402765568 + 119370240},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
-    "bwd_train": {"src": "57502e753943cca5", "bytes": 405177856 + 230648576},
+    "bwd_train": {"src": "f03ac3c4b07889e1", "bytes": 405157376 + 224179968},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
     # proportional to B, stored here scaled to the B=64 launch
-    "decode_split": {"src": "901f9d8b8d4d9813", "bytes": (1073857000 + 6977280) * 8},
+    "decode_split": {"src": "a53655af1af4de31", "bytes": (1073855000 + 7006208) * 8},
 }
 
 
@@ -484,7 +484,7 @@ def run_ours(args, ws, rank, local):
                    "inputs": "torch.randn (seeded Philox) on the device, rounded to bf16"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                     "kernel": "fwd_bf16_kernel<128>",
+                     "kernel": "fwd_kernel<128, false>",
                      "traffic": traffic_for("fwd_prefill", ("fa_fwd.cu", "sm103.cuh"))},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
