@@ -21,17 +21,22 @@
 //   tensor order: Sᵀ_0 dPᵀ_0 dV_0 Sᵀ_1 dK_0 dQ_0 dPᵀ_1 dV_1 Sᵀ_2 dK_1 dQ_1 …
 // dQ_i is added into an fp32 accumulator in global memory (kernel 3 scales it
 // by σ and converts it to bf16).  It is computed transposed (both operands read
-// MN-major from the K_j and dSᵀ tiles) so that TMEM lane = head-dim index: a
-// warp then adds 32 consecutive head-dim values of one query row, one full
-// 128-byte line per reduction instruction.
+// MN-major from the K_j and dSᵀ tiles) so that TMEM lane = head-dim index; a
+// 4 × 4 exchange among neighbouring lanes then gives each lane four consecutive
+// head dims of one query row, and every 16-byte-per-lane reduction covers four
+// full 128-byte lines.  Those reductions (as many bytes as the whole fp32 dQ
+// once per key tile) are what the L2 has to absorb, so two warpgroups issue
+// them, each for half of the query columns.
 //
 // Causal mask (query i sees key j when j <= i): key tile j only meets query
 // tiles i >= j, so the loop starts at its diagonal tile, where Pᵀ entries with
 // key > query are zeroed (and with them dSᵀ).
 //
-// Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner + MMA issuer;
-// warps 2..5 compute Pᵀ and dSᵀ (thread = key row) and write dK/dV at the end;
-// warps 6..9 drain dQ_iᵀ from TMEM (thread = head-dim index) into the accumulator.
+// Warp roles (512 threads, four warpgroups, registers rebalanced with
+// setmaxnreg): warp 0 TMA producer and warp 1 TMEM owner + MMA issuer (warps 2,
+// 3 idle); warps 4..7 compute Pᵀ and dSᵀ (thread = key row) and write dK/dV at
+// the end; warps 8..11 and 12..15 drain dQ_iᵀ columns 0..63 and 64..127 from
+// TMEM (thread = head-dim index) into the accumulator.
 // TMEM columns: Sᵀ (then Pᵀ in 0..63) 0..127, dPᵀ (then dQ_iᵀ) 128..255,
 // dV 256..383, dK 384..511.
 #include "fa_kernels.h"
@@ -44,7 +49,17 @@ constexpr int kD = 128;
 constexpr int kTile = 128;
 constexpr int kTileBytes = 128 * 128;   // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kOpBytes = 2 * kTileBytes;  // one 128 × 128 bf16 operand
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;  // four warpgroups: control, compute, two dQ drains
+// Register split (setmaxnreg): the kernel launches with kRegsLaunch per thread
+// (all ptxas allows for 512 threads); the control and drain warpgroups give
+// registers to the compute warpgroup.  Each sub-partition holds one warp of
+// every warpgroup, so the split must fit 512 × kRegsLaunch; the launcher
+// refuses to run if ptxas assigned fewer registers than that.
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsControl = 80;
+constexpr int kRegsCompute = 224;
+constexpr int kRegsDrain = 104;
+static_assert(128 * (kRegsControl + kRegsCompute + 2 * kRegsDrain) <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
@@ -72,6 +87,72 @@ __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernBwd 
 
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Bounded mbarrier wait with the polling loop inlined: warps whose register
+// limit was lowered cannot call the out-of-line slow path.
+__device__ __forceinline__ bool mbar_wait_inl(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned int* err, unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        atomicCAS(err, 0u, code);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_drain_inl(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+// Adds 32 columns of dQᵀ (this lane's head dim, columns cbase … cbase+31) into
+// the fp32 accumulator rows: per block of four columns, a 4 × 4 exchange among
+// lanes 4g … 4g+3 gives lane 4g + r4 column c0 + r4 for head dims 4g … 4g+3,
+// added with one 16-byte reduction.  dst points at head dim 4g of row 0.
+__device__ __forceinline__ void reduce_cols(const uint32_t (&v)[32], float* dst, int cbase, int r4) {
+#pragma unroll
+  for (int c0 = 0; c0 < 32; c0 += 4) {
+    float a0 = __uint_as_float(v[c0]), a1 = __uint_as_float(v[c0 + 1]);
+    float a2 = __uint_as_float(v[c0 + 2]), a3 = __uint_as_float(v[c0 + 3]);
+    {
+      const bool o = r4 & 1;  // swap the odd/even halves of each lane pair
+      const float y0 = __shfl_xor_sync(0xffffffffu, o ? a0 : a1, 1);
+      const float y1 = __shfl_xor_sync(0xffffffffu, o ? a2 : a3, 1);
+      if (o) { a0 = y0; a2 = y1; } else { a1 = y0; a3 = y1; }
+    }
+    {
+      const bool o = r4 & 2;  // then the 2 × 2 blocks of each lane quad
+      const float y0 = __shfl_xor_sync(0xffffffffu, o ? a0 : a2, 2);
+      const float y1 = __shfl_xor_sync(0xffffffffu, o ? a1 : a3, 2);
+      if (o) { a0 = y0; a1 = y1; } else { a2 = y0; a3 = y1; }
+    }
+    float* q = dst + static_cast<int64_t>(cbase + c0 + r4) * kD;
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(q), "f"(a0), "f"(a1), "f"(a2), "f"(a3)
+                 : "memory");
+  }
 }
 
 // ---------------------------------------------------------------- kernel 1
@@ -160,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->dq_free, 256);
     mbar_init(&bars->p_ready, 128);
     mbar_init(&bars->ds_ready, 128);
     mbar_init(&bars->ds_free, 1);
@@ -178,7 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
+  if (warp < 4) {
+    // Control warpgroup (producer, MMA issuer, two idle warps) gives registers
+    // to the compute warpgroup; every role ends at the same named barrier,
+    // after which the MMA warp frees TMEM.
+    reg_dealloc<kRegsControl>();
+    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -194,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       for (int it = 0; it < nT; ++it) {
         const int i = i0 + it;
         const int qb = it & 1;
-        if (!mbar_wait(&bars->q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        if (!mbar_wait_inl(&bars->q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.err, site(1))) break;
         mbar_arrive_expect_tx(&bars->q_full[qb], 2 * kOpBytes);
         for (int kb = 0; kb < 2; ++kb) {
           tma_load_4d(smem + kOffQ + qb * kOpBytes + kb * kTileBytes, &p.tm_q, &bars->q_full[qb], kb * 64,
@@ -205,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         ++issued;
       }
       if (*abort_flag) {
-        mbar_wait_drain(&bars->kv_full, 0, 200000000ull);
+        mbar_wait_drain_inl(&bars->kv_full, 0, 200000000ull);
         for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
-          mbar_wait_drain(&bars->q_full[t & 1], (t >> 1) & 1, 200000000ull);
+          mbar_wait_drain_inl(&bars->q_full[t & 1], (t >> 1) & 1, 200000000ull);
       }
     }
-  } else if (warp == 1) {
+    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // Sᵀ, dPᵀ
@@ -229,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         }
         mma_commit(&bars->s_full);
       };
-      bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, site(2)) &&
-                mbar_wait(&bars->q_full[0], 0, abort_flag, p.err, site(3));
+      bool ok = mbar_wait_inl(&bars->kv_full, 0, abort_flag, p.err, site(2)) &&
+                mbar_wait_inl(&bars->q_full[0], 0, abort_flag, p.err, site(3));
       if (ok) {
         tc_fence_after();
         issue_st(0);
@@ -240,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         const uint32_t dob = sDO + (it & 1) * kOpBytes;
         const uint32_t qb = sQ + (it & 1) * kOpBytes;
         // dPᵀ_i = V_j dO_iᵀ into columns that held dQ_{i−1}: wait until it is drained.
-        if (!(ok = mbar_wait(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(4)))) break;
+        if (!(ok = mbar_wait_inl(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(4)))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -250,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         }
         mma_commit(&bars->dp_full);
         // dV += Pᵀ dO_i with Pᵀ (bf16 pairs) read from TMEM columns 0..63.
-        if (!(ok = mbar_wait(&bars->p_ready, ph, abort_flag, p.err, site(5)))) break;
+        if (!(ok = mbar_wait_inl(&bars->p_ready, ph, abort_flag, p.err, site(5)))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
@@ -258,11 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                       (it > 0 || kk > 0) ? 1u : 0u);
         // Sᵀ_{i+1} overwrites Pᵀ_i, which the dV MMAs above read first (in order).
         if (it + 1 < nT) {
-          if (!(ok = mbar_wait(&bars->q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort_flag, p.err, site(6)))) break;
+          if (!(ok = mbar_wait_inl(&bars->q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort_flag, p.err, site(6)))) break;
           tc_fence_after();
           issue_st(it + 1);
         }
-        if (!(ok = mbar_wait(&bars->ds_ready, ph, abort_flag, p.err, site(7)))) break;
+        if (!(ok = mbar_wait_inl(&bars->ds_ready, ph, abort_flag, p.err, site(7)))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {  // dK += dSᵀ Q_i
@@ -281,14 +367,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       mma_commit(&bars->acc_done);
       if (*abort_flag) {
         mma_commit(&bars->drain);
-        mbar_wait_drain(&bars->drain, 0, 200000000ull);
+        mbar_wait_drain_inl(&bars->drain, 0, 200000000ull);
       }
     }
-  } else if (warp < 6) {
+    }
+    tc_fence_before();
+    named_sync(2, kThreads);
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+  } else if (warp < 8) {
+    reg_alloc<kRegsCompute>();
     // -------------------------------------------- Pᵀ / dSᵀ, then dK / dV out
     const int wq = warp & 3;
     const int r = wq * 32 + lane;             // key row within the tile
-    const int tr = threadIdx.x - 64;          // 0..127, for staging row stats
+    const int tr = threadIdx.x - 128;         // 0..127, for staging row stats
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     uint8_t* sDST = smem + kOffDST;
@@ -405,45 +499,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         }
       }
     }
+    tc_fence_before();
+    named_sync(2, kThreads);
   } else {
+    reg_dealloc<kRegsDrain>();
     // ------------------------------------------------------ dQ_iᵀ drain
+    // Two warpgroups, each owning 64 of dQ_iᵀ's 128 query columns.  A 4 × 4
+    // exchange among neighbouring lanes turns "lane = head-dim index" into four
+    // consecutive head dims of one query row per lane, so every reduction
+    // instruction adds 16 bytes per lane: four full 128-byte lines per warp.
+    const int half = (warp - 8) >> 2;
     const int wq = warp & 3;
-    const int dcol = wq * 32 + lane;  // head-dim index (TMEM lane)
+    const int r4 = lane & 3;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     for (int it = 0; it < nT; ++it) {
       const int i = i0 + it;
-      const bool ok = mbar_wait(&bars->dq_full, it & 1, abort_flag, p.err, site(12));
+      const bool ok = mbar_wait_inl(&bars->dq_full, it & 1, abort_flag, p.err, site(12));
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tmem + lane_base + kColDP + 0, r0);
-      tmem_ld32(tmem + lane_base + kColDP + 32, r1);
-      tmem_ld32(tmem + lane_base + kColDP + 64, r2);
-      tmem_ld32(tmem + lane_base + kColDP + 96, r3);
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem + lane_base + kColDP + half * 64, r0);
+      tmem_ld32(tmem + lane_base + kColDP + half * 64 + 32, r1);
       tmem_wait_ld();
       reg_fence(r0);
       reg_fence(r1);
-      reg_fence(r2);
-      reg_fence(r3);
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
-      // Column c of dQ_iᵀ is query row i·128 + c; lanes cover consecutive head dims.
-      float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * kD + dcol;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        atomicAdd(dst + (c + 0) * kD, __uint_as_float(r0[c]));
-        atomicAdd(dst + (c + 32) * kD, __uint_as_float(r1[c]));
-        atomicAdd(dst + (c + 64) * kD, __uint_as_float(r2[c]));
-        atomicAdd(dst + (c + 96) * kD, __uint_as_float(r3[c]));
-      }
+      // Column c of dQ_iᵀ is query row i·128 + c; lane 4g + r4 ends up with query
+      // row c0 + r4, head dims wq·32 + 4g … +3.
+      float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * kD + wq * 32 + (lane & ~3);
+      reduce_cols(r0, dst, half * 64, r4);
+      reduce_cols(r1, dst, half * 64 + 32, r4);
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tc_fence_before();
+    named_sync(2, kThreads);
   }
 }
 
@@ -461,6 +550,11 @@ cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t stream, int*
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
     return e;
+  // setmaxnreg.inc waits until the block's pool can supply the registers: refuse
+  // to launch unless ptxas gave the kernel the count the split assumes.
+  cudaFuncAttributes attr;
+  if ((e = cudaFuncGetAttributes(&attr, bwd_main_kernel)) != cudaSuccess) return e;
+  if (attr.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
   bwd_main_kernel<<<dim3(p.N / kTile, p.H, p.B), kThreads, kSmem, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
