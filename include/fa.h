@@ -12,7 +12,7 @@
  * end, so the N×N score and probability matrices never reach device memory.
  *
  * Conventions shared by every entry point.
- *   - Tensors are device pointers.  Q, K, V, O, dO, dQ, dK, dV are
+ *   - Tensors are device pointers (fa_forward_host alone takes host ones).  Q, K, V, O, dO, dQ, dK, dV are
  *     [B, H, N, d] row-major with d innermost, the shape "Q, K, V ∈ R^{N×d}"
  *     of the FlashAttention walkthrough (kyonqi.github.io, "Flash Attention
  *     Forward") with batch and head dims in front.  LSE is [B, H, N] float32.
@@ -109,6 +109,41 @@ FA_API fa_status fa_forward_masked(const void* q, const void* k, const void* v, 
 FA_API fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int B, int H, int N_q, int N_kv, int d, float scale, float q_descale,
                                 float k_descale, float v_descale, fa_mask mask, void* stream);
+
+/*
+ * fa_forward_host_workspace_size — device bytes fa_forward_host needs for the
+ *   same arguments: two chunk buffers, each holding q [heads,N_q,d], k and v
+ *   [heads,N_kv,d], o [heads,N_q,d] (element size of dtype) and lse [heads,N_q]
+ *   float32 for `heads` = min(heads_per_chunk, B·H) (heads_per_chunk = 0: the
+ *   chunk fa_forward_host picks on the current device), every piece rounded up
+ *   to 256 bytes.  Returns 0 for invalid sizes or dtype, or when
+ *   heads_per_chunk = 0 and no device can be queried.
+ */
+FA_API size_t fa_forward_host_workspace_size(int B, int H, int N_q, int N_kv, int d, fa_dtype dtype,
+                                             int heads_per_chunk);
+
+/*
+ * fa_forward_host — fa_forward_masked on HOST tensors.  The lesson states the
+ *   forward on HBM-resident Q, K, V (§1–§3); this entry point adds the transfer
+ *   to and from host memory, which it does not cover.  q, k, v, o,
+ *   lse are host pointers to contiguous [B,H,N,d] tensors (lse [B,H,N_q]
+ *   float32, may be NULL), preferably page-locked: copies from pageable memory
+ *   are correct but do not overlap.  The B·H heads are processed in chunks of
+ *   heads_per_chunk (0 = let the library choose) through two device buffers in
+ *   `workspace` (>= fa_forward_host_workspace_size bytes, 256-byte aligned,
+ *   owned by the caller): the copy of chunk c+1 in, the forward on chunk c and
+ *   the copy of chunk c−1 out run concurrently on two library-owned copy
+ *   streams and `stream`, ordered after the work already queued on `stream`.
+ *   The call returns once everything is queued; o and lse are valid after
+ *   `stream` has been synchronised.  Results equal fa_forward_masked's on the
+ *   same data.  Calls on one device are serialised internally.  Argument errors
+ *   return FA_ERR_INVALID_ARG before anything is queued; dtype, d and mask as
+ *   for fa_forward_masked.
+ */
+FA_API fa_status fa_forward_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int N_q, int N_kv, int d, fa_dtype dtype, float scale,
+                                 fa_mask mask, int heads_per_chunk, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /*
  * fa_decode_workspace_size — bytes of workspace fa_decode_splitkv needs:

@@ -1,6 +1,9 @@
 // fa_api.cu — the C ABI declared in include/fa.h: argument checks, TMA
 // descriptor construction and kernel dispatch.  No device memory is allocated
-// here; every buffer, including workspaces, belongs to the caller.
+// here; every buffer, including workspaces, belongs to the caller.  The only
+// resources the library creates are, per device, the two copy streams and the
+// events fa_forward_host pipelines its transfers with.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -279,6 +282,181 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, f
   cudaError_t e = fa::launch_fwd_fp8(d, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_forward_fp8 launch");
   return check_launch("fa_forward_fp8", 1);
+}
+
+}  // extern "C"
+
+namespace {
+
+// ------------------------------------------------ host-buffer forward
+// Per-device copy streams and events for fa_forward_host, created on first use
+// and kept for the life of the process.  The mutex serialises calls on one
+// device: they share the events (a stream wait captures the event's latest
+// record when it is queued, so reuse across chunks and calls is safe).
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  int sms = 1;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t in_done[2] = {nullptr, nullptr};   // chunk's q, k, v are on the device
+  cudaEvent_t fwd_done[2] = {nullptr, nullptr};  // chunk's forward has finished
+  cudaEvent_t out_done[2] = {nullptr, nullptr};  // chunk's o, lse are back on the host
+};
+HostPipe g_pipes[64];
+
+fa_status init_pipe(HostPipe& hp, int dev) {
+  cudaError_t e;
+  if ((e = cudaDeviceGetAttribute(&hp.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e, "fa_forward_host: SM count");
+  if ((e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess)
+    return cuda_fail(e, "fa_forward_host: stream/event creation");
+  for (int b = 0; b < 2; ++b) {
+    if ((e = cudaEventCreateWithFlags(&hp.in_done[b], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.fwd_done[b], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.out_done[b], cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e, "fa_forward_host: event creation");
+  }
+  hp.ready = true;
+  return FA_OK;
+}
+
+// Byte offsets of one chunk buffer inside the workspace.
+struct HostChunk {
+  size_t q, k, v, o, lse, bytes;
+};
+
+HostChunk host_chunk(int N_q, int N_kv, int d, int esz, int heads) {
+  HostChunk c;
+  const size_t hq = static_cast<size_t>(heads) * N_q * d * esz, hk = static_cast<size_t>(heads) * N_kv * d * esz;
+  c.q = 0;
+  c.k = c.q + round256(hq);
+  c.v = c.k + round256(hk);
+  c.o = c.v + round256(hk);
+  c.lse = c.o + round256(hq);
+  c.bytes = c.lse + round256(static_cast<size_t>(heads) * N_q * 4);
+  return c;
+}
+
+// Heads per chunk: the caller's choice, or about eight chunks with at least
+// two waves of 256-row blocks each.
+int64_t chunk_heads(int64_t heads, int N_q, int requested, int sms) {
+  int64_t hpc = requested;
+  if (hpc == 0) {
+    const int64_t blocks_per_head = (N_q + 255) / 256;
+    hpc = std::max<int64_t>((heads + 7) / 8, (2 * static_cast<int64_t>(sms) + blocks_per_head - 1) / blocks_per_head);
+  }
+  return std::min<int64_t>(std::min<int64_t>(hpc, heads), 65535);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_forward_host_workspace_size(int B, int H, int N_q, int N_kv, int d, fa_dtype dtype, int heads_per_chunk) {
+  if (B <= 0 || H <= 0 || N_q <= 0 || N_kv <= 0 || d <= 0 || heads_per_chunk < 0) return 0;
+  if (dtype != FA_BF16 && dtype != FA_FP32) return 0;
+  int sms = 1;
+  if (heads_per_chunk == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 0;
+  }
+  const int64_t hpc = chunk_heads(static_cast<int64_t>(B) * H, N_q, heads_per_chunk, sms);
+  return 2 * host_chunk(N_q, N_kv, d, dtype == FA_BF16 ? 2 : 4, static_cast<int>(hpc)).bytes;
+}
+
+fa_status fa_forward_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N_q,
+                          int N_kv, int d, fa_dtype dtype, float scale, fa_mask mask, int heads_per_chunk,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  // Every check fa_forward_masked makes on a chunk is made here first, so a
+  // bad argument returns before any copy is queued.
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_forward_host: null tensor pointer");
+  if (!workspace) return fail(FA_ERR_INVALID_ARG, "fa_forward_host: null workspace");
+  if (B <= 0 || H <= 0 || N_q <= 0 || N_kv <= 0 || d <= 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_host: sizes must be positive (B=%d H=%d N_q=%d N_kv=%d d=%d)", B, H,
+                N_q, N_kv, d);
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_forward_host: unknown dtype %d", dtype);
+  if (mask != FA_MASK_NONE && mask != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_host: unknown mask %d", static_cast<int>(mask));
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_forward_host: head dim %d not built (64, 128)", d);
+  if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_forward_host: scale must be finite and > 0");
+  if (mask == FA_MASK_CAUSAL && N_q > N_kv)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_host: causal attention needs N_q <= N_kv (got %d > %d)", N_q, N_kv);
+  if (heads_per_chunk < 0) return fail(FA_ERR_INVALID_ARG, "fa_forward_host: heads_per_chunk must be >= 0");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_host: workspace must be 256-byte aligned");
+  const int64_t heads = static_cast<int64_t>(B) * H;
+  const int esz = dtype == FA_BF16 ? 2 : 4;
+  if (heads_per_chunk > 0) {  // the size is known without asking the device
+    const int hpc = static_cast<int>(chunk_heads(heads, N_q, heads_per_chunk, 1));
+    const size_t need = 2 * host_chunk(N_q, N_kv, d, esz, hpc).bytes;
+    if (workspace_bytes < need)
+      return fail(FA_ERR_INVALID_ARG, "fa_forward_host: workspace of %zu bytes is smaller than the %zu needed",
+                  workspace_bytes, need);
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  HostPipe& hp = g_pipes[dev];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  if (!hp.ready) {
+    fa_status r = init_pipe(hp, dev);
+    if (r != FA_OK) return r;
+  }
+  const int64_t hpc = chunk_heads(heads, N_q, heads_per_chunk, hp.sms);
+  const HostChunk L = host_chunk(N_q, N_kv, d, esz, static_cast<int>(hpc));
+  if (workspace_bytes < 2 * L.bytes)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_host: workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, 2 * L.bytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t q_head = static_cast<size_t>(N_q) * d * esz, kv_head = static_cast<size_t>(N_kv) * d * esz;
+  const int64_t chunks = (heads + hpc - 1) / hpc;
+#define FA_HOST_CUDA(call, what)                  \
+  do {                                            \
+    cudaError_t ce_ = (call);                     \
+    if (ce_ != cudaSuccess) return cuda_fail(ce_, what); \
+  } while (0)
+  FA_HOST_CUDA(cudaEventRecord(hp.start, s), "fa_forward_host: event record");
+  FA_HOST_CUDA(cudaStreamWaitEvent(hp.h2d, hp.start, 0), "fa_forward_host: stream wait");
+  FA_HOST_CUDA(cudaStreamWaitEvent(hp.d2h, hp.start, 0), "fa_forward_host: stream wait");
+  for (int64_t c = 0; c < chunks; ++c) {
+    const int b = static_cast<int>(c & 1);
+    const int64_t h0 = c * hpc;
+    const int nh = static_cast<int>(std::min<int64_t>(hpc, heads - h0));
+    uint8_t* buf = ws + b * L.bytes;
+    // Buffer b was last used by chunk c − 2: its results must be home first.
+    if (c >= 2) FA_HOST_CUDA(cudaStreamWaitEvent(hp.h2d, hp.out_done[b], 0), "fa_forward_host: stream wait");
+    FA_HOST_CUDA(cudaMemcpyAsync(buf + L.q, static_cast<const uint8_t*>(q) + h0 * q_head, nh * q_head,
+                                 cudaMemcpyHostToDevice, hp.h2d), "fa_forward_host: copy q in");
+    FA_HOST_CUDA(cudaMemcpyAsync(buf + L.k, static_cast<const uint8_t*>(k) + h0 * kv_head, nh * kv_head,
+                                 cudaMemcpyHostToDevice, hp.h2d), "fa_forward_host: copy k in");
+    FA_HOST_CUDA(cudaMemcpyAsync(buf + L.v, static_cast<const uint8_t*>(v) + h0 * kv_head, nh * kv_head,
+                                 cudaMemcpyHostToDevice, hp.h2d), "fa_forward_host: copy v in");
+    FA_HOST_CUDA(cudaEventRecord(hp.in_done[b], hp.h2d), "fa_forward_host: event record");
+    FA_HOST_CUDA(cudaStreamWaitEvent(s, hp.in_done[b], 0), "fa_forward_host: stream wait");
+    fa_status r = forward_impl(buf + L.q, buf + L.k, buf + L.v, buf + L.o,
+                               lse ? reinterpret_cast<float*>(buf + L.lse) : nullptr, 1, nh, N_q, N_kv, d, dtype,
+                               scale, nullptr, mask == FA_MASK_CAUSAL ? 1 : 0, s);
+    if (r != FA_OK) return r;
+    FA_HOST_CUDA(cudaEventRecord(hp.fwd_done[b], s), "fa_forward_host: event record");
+    FA_HOST_CUDA(cudaStreamWaitEvent(hp.d2h, hp.fwd_done[b], 0), "fa_forward_host: stream wait");
+    FA_HOST_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(o) + h0 * q_head, buf + L.o, nh * q_head,
+                                 cudaMemcpyDeviceToHost, hp.d2h), "fa_forward_host: copy o out");
+    if (lse)
+      FA_HOST_CUDA(cudaMemcpyAsync(lse + h0 * N_q, buf + L.lse, static_cast<size_t>(nh) * N_q * 4,
+                                   cudaMemcpyDeviceToHost, hp.d2h), "fa_forward_host: copy lse out");
+    FA_HOST_CUDA(cudaEventRecord(hp.out_done[b], hp.d2h), "fa_forward_host: event record");
+  }
+  // The copy-out stream runs the chunks in order: its last event covers them all.
+  FA_HOST_CUDA(cudaStreamWaitEvent(s, hp.out_done[(chunks - 1) & 1], 0), "fa_forward_host: stream wait");
+#undef FA_HOST_CUDA
+  return ok();
 }
 
 size_t fa_decode_workspace_size(int B, int H, int d, int n_splits) {

@@ -25,6 +25,8 @@ EXPORTED = (
     "fa_forward",
     "fa_forward_masked",
     "fa_forward_fp8",
+    "fa_forward_host_workspace_size",
+    "fa_forward_host",
     "fa_decode_workspace_size",
     "fa_decode_splitkv",
     "fa_decode_splitkv_gqa",
@@ -65,6 +67,10 @@ def lib() -> ctypes.CDLL:
         L.fa_forward_masked.restype = i32
         L.fa_forward_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32, f32, i32, vp]
         L.fa_forward_fp8.restype = i32
+        L.fa_forward_host_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        L.fa_forward_host_workspace_size.restype = sz
+        L.fa_forward_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, sz, vp]
+        L.fa_forward_host.restype = i32
         L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fa_decode_workspace_size.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
@@ -170,6 +176,52 @@ def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse:
     else:
         _check(lib().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d,
                                 _dtype_code(q), float(scale), strides, _stream_ptr(stream)))
+    return out, lse
+
+
+_host_ws = {}
+
+
+def forward_host(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool = False,
+                 heads_per_chunk: int = 0, device=None, stream=None):
+    """Forward on host tensors: q [B,H,Nq,d], k/v [B,H,Nkv,d] contiguous CPU
+    tensors (bf16 or fp32; page-locked ones let the copies overlap).  The
+    library streams (b, h) chunks through a device workspace, overlapping the
+    copies in and out with the forward.  Returns (O, LSE) as CPU tensors
+    (page-locked when allocated here); they are valid once ``stream`` (default:
+    the device's current stream) has been synchronised."""
+    torch = _torch()
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("forward_host takes contiguous CPU tensors")
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    if k.shape != (B, H, Nkv, d) or v.shape != (B, H, Nkv, d):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=True)
+    for t in (out, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("out and lse must be contiguous CPU tensors")
+    code = _dtype_code(q)
+    with torch.cuda.device(dev):
+        need = int(lib().fa_forward_host_workspace_size(B, H, Nq, Nkv, d, code, int(heads_per_chunk)))
+        if need == 0:
+            raise FAError(FA_ERR_INVALID_ARG, "fa_forward_host_workspace_size rejected the arguments")
+        ws = _host_ws.get(dev.index)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            _host_ws[dev.index] = ws
+        _check(lib().fa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d, code,
+                                     float(scale), FA_MASK_CAUSAL if causal else FA_MASK_NONE,
+                                     int(heads_per_chunk), _ptr(ws), ws.numel(), _stream_ptr(stream)))
     return out, lse
 
 

@@ -156,3 +156,35 @@ def test_paged_decode_validates_before_cuda(L):
     assert dec(table=None) == fa.FA_ERR_INVALID_ARG
     assert dec(wsb=16) == fa.FA_ERR_INVALID_ARG
     assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_host_forward_workspace_size(L):
+    # 3 heads of N_q=100, N_kv=300, d=128 bf16: q 76800 B, k and v 230400 B each, o 76800 B,
+    # lse 1200 B -> 1280 B (each piece rounded up to 256 bytes); two chunk buffers.
+    per_chunk = 76800 + 2 * 230400 + 76800 + 1280
+    assert L.fa_forward_host_workspace_size(2, 4, 100, 300, 128, fa.FA_BF16, 3) == 2 * per_chunk
+    # A chunk larger than B·H is clamped to B·H heads.
+    assert (L.fa_forward_host_workspace_size(1, 2, 64, 64, 64, fa.FA_FP32, 50)
+            == L.fa_forward_host_workspace_size(1, 2, 64, 64, 64, fa.FA_FP32, 2))
+    assert L.fa_forward_host_workspace_size(0, 2, 64, 64, 64, fa.FA_BF16, 1) == 0
+    assert L.fa_forward_host_workspace_size(1, 2, 64, 64, 64, 9, 1) == 0
+    assert L.fa_forward_host_workspace_size(1, 2, 64, 64, 64, fa.FA_BF16, -1) == 0
+
+
+def test_host_forward_validates_before_cuda(L):
+    def fh(q=FAKE, ws=FAKE, B=2, H=3, nq=128, nkv=128, d=128, dt=fa.FA_BF16, scale=0.1, mask=fa.FA_MASK_NONE,
+           hpc=2, wsb=1 << 30):
+        return L.fa_forward_host(q, FAKE, FAKE, FAKE, None, B, H, nq, nkv, d, dt, scale, mask, hpc, ws, wsb, None)
+    assert fh(q=None) == fa.FA_ERR_INVALID_ARG
+    assert fh(ws=None) == fa.FA_ERR_INVALID_ARG
+    assert fh(B=0) == fa.FA_ERR_INVALID_ARG
+    assert fh(dt=7) == fa.FA_ERR_INVALID_ARG
+    assert fh(mask=3) == fa.FA_ERR_INVALID_ARG
+    assert fh(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fh(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert fh(mask=fa.FA_MASK_CAUSAL, nq=200, nkv=100) == fa.FA_ERR_INVALID_ARG
+    assert fh(hpc=-1) == fa.FA_ERR_INVALID_ARG
+    assert fh(ws=FAKE_BAD) == fa.FA_ERR_INVALID_ARG
+    need = L.fa_forward_host_workspace_size(2, 3, 128, 128, 128, fa.FA_BF16, 2)
+    assert fh(wsb=need - 1) == fa.FA_ERR_INVALID_ARG
+    assert b"workspace" in L.fa_get_last_error()
