@@ -704,6 +704,8 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
     return r;
   t.block_table = block_table;
   t.seq_lens = seq_lens;
+  t.k_pages = k_cache;
+  t.v_pages = v_cache;
   t.max_blocks = max_blocks;
   t.block_size = block_size;
   t.num_blocks = num_blocks;

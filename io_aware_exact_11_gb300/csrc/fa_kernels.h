@@ -70,6 +70,8 @@ struct DecodeTcParams {
   CUtensorMap tm_v;
   const int* block_table;  // paged cache only: [B, max_blocks]
   const int* seq_lens;     // paged cache only: [B]
+  const void* k_pages;     // paged cache only: [num_blocks, Hkv, bs, d] bf16 (copied per thread for small pages)
+  const void* v_pages;
   int max_blocks, block_size, num_blocks;
   float* part_o;     // [B,Hq,S,d] fp32
   float* part_ml;    // [B,Hq,S,2] fp32

@@ -89,14 +89,16 @@ def _run(seed, B, Hq, Hkv, lens, bs, splits, heads=None):
     (2, 28, 4, [513, 777], 64, 4),
     (2, 8, 4, [128, 1200], 128, 16),         # groups of 2, one page per tile
     (1, 8, 1, [700], 32, 1),                 # one key/value head, one split
+    (1, 8, 2, [17000], 16, 1),               # 1063 pages in one split: past the 1024 staged page ids
 ])
 def test_paged_decode_matches_oracle(B, Hq, Hkv, lens, bs, splits):
     _run(41, B, Hq, Hkv, lens, bs, splits)
 
 
-def test_paged_decode_flags_a_bad_page_id_without_faulting():
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4)])   # single-head kernel; grouped kernel's copy warps
+def test_paged_decode_flags_a_bad_page_id_without_faulting(Hq, Hkv):
     import torch
-    q, kc, vc, table, lens = _paged(42, 1, 4, 4, [300], 16)
+    q, kc, vc, table, lens = _paged(42, 1, Hq, Hkv, [300], 16)
     table[0, 3] = 10 ** 6
     with pytest.raises(fa.FAError) as ei:
         fa.decode_paged(to_device(q[:, :, None, :].copy(), "bf16"), to_device(kc, "bf16"), to_device(vc, "bf16"),
