@@ -14,8 +14,12 @@
 //
 // Warp roles (96 threads): warp 0 softmax for TMEM lanes 0..31 (rows 0..31 of
 // the A tile; rows ≥ G are padding) and the epilogue; warp 1 TMA producer
-// (Q once, then K_0, K_1, V_0, K_2, V_1, … into a 3-slot ring); warp 2 TMEM
+// (Q once, then K_0, K_1, V_0, K_2, V_1, … into a 5-slot ring); warp 2 TMEM
 // owner and MMA issuer.  TMEM: S buffers at columns 0 and 128, O at 256.
+// P̃ is written as bf16 pairs over its S buffer and read from TMEM by the P̃V
+// MMA; S(j) is issued after P̃V(j−2), so the in-order tensor pipe has read
+// P̃(j−2) before S(j) overwrites it.  Keeping P̃ out of shared memory leaves
+// room for five ring slots, which is what keeps enough copies in flight.
 // Rows keep their reference max until a tile's max exceeds it by 2^8 (base 2),
 // exactly as in the forward kernel; the merge accepts any reference m.
 //
@@ -42,7 +46,7 @@ namespace {
 constexpr int kBN = 128;
 constexpr int kTileBytes = 128 * 128;    // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kSlot = 2 * kTileBytes;    // one 128 × 128 bf16 tile
-constexpr int kRing = 3;
+constexpr int kRing = 5;
 constexpr int kThreads = 96;
 constexpr int kLoaderThreads = 128;  // the LOADER variant's copy warps (warps 3..6)
 constexpr uint32_t kTmemCols = 512;
@@ -51,8 +55,7 @@ constexpr float kRescaleLog2 = 8.0f;
 
 constexpr int kOffQ = 0;
 constexpr int kOffR = kOffQ + kSlot;
-constexpr int kOffP = kOffR + kRing * kSlot;
-constexpr int kOffPages = kOffP + kSlot;       // paged cache: staged page ids
+constexpr int kOffPages = kOffR + kRing * kSlot;  // paged cache: staged page ids
 constexpr int kMaxStagedPages = 1024;
 constexpr int kOffBar = kOffPages + kMaxStagedPages * 4;
 constexpr int kSmem = kOffBar + 256 + 1024;
@@ -230,7 +233,6 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
       constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, false, true);
       const uint32_t sQ = smem_u32(smem + kOffQ);
       const uint32_t sR = smem_u32(smem + kOffR);
-      const uint32_t sP = smem_u32(smem + kOffP);
       auto issue_pv = [&](int jj) -> bool {
         const int t = seq_v(jj, T);
         const int slot = t % kRing;
@@ -239,9 +241,9 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
         tc_fence_after();
         const uint32_t vb = sR + slot * kSlot;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ss(tmem + kColO, sdesc_sw128(sP + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
-                      sdesc_sw128(vb + kk * 2048, kTileBytes, 1024), kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk)  // A = P̃(jj) from its S buffer's TMEM columns
+          mma_bf16_ts(tmem + kColO, tmem + (jj & 1) * kBN + kk * 8, sdesc_sw128(vb + kk * 2048, kTileBytes, 1024),
+                      kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->p_free);
         mma_commit(&bars->r_empty[slot]);
         return true;
@@ -310,7 +312,6 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
     // ------------------------------------------- softmax for rows 0..31, epilogue
     const int row = lane;  // TMEM lane; rows < G are the group's query heads
     const float sl2 = p.scale_log2;
-    uint8_t* sP = smem + kOffP;
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
@@ -371,17 +372,21 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
         }
       l_run = l_run * corr + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
 
+      {
+        uint32_t w0[32], w1[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          w0[e] = pack_bf16x2(s[2 * e], s[2 * e + 1]);
+          w1[e] = pack_bf16x2(s[64 + 2 * e], s[64 + 2 * e + 1]);
+        }
+        tmem_st32(tmem + sb * kBN, w0);
+        tmem_st32(tmem + sb * kBN + 32, w1);
+      }
+      // Wait for P̃V(j−1) on every tile, not only before a rescale of O: the
+      // final wait below tells phases apart by parity, which is only sound if
+      // p_free is never more than one phase ahead of the last one waited for.
       ok = mbar_wait(&bars->p_free, (j & 1) ^ 1, abort_flag, p.err, site(8));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint4 v;
-        v.x = pack_bf16x2(s[8 * c8 + 0], s[8 * c8 + 1]);
-        v.y = pack_bf16x2(s[8 * c8 + 2], s[8 * c8 + 3]);
-        v.z = pack_bf16x2(s[8 * c8 + 4], s[8 * c8 + 5]);
-        v.w = pack_bf16x2(s[8 * c8 + 6], s[8 * c8 + 7]);
-        *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kTileBytes + row * 128 + (((c8 & 7) ^ (row & 7)) << 4)) = v;
-      }
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
         tc_fence_after();
 #pragma unroll
@@ -395,8 +400,8 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
           tmem_st32(oa, r);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
       if (PAGED && !LOADER && valid < kBN) {
         // Zero the V rows past the sequence end once V_j has landed.
         const int t = seq_v(j, T);
