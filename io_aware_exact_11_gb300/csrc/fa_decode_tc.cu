@@ -153,7 +153,55 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
       }
       __syncwarp();
     }
-    if (lane == 0 && T > 0) {
+    // Page holding key t0 (a multiple of the page size), checked.
+    auto page_id = [&](int t0) -> int {
+      const int rel = t0 / p.block_size - page0;
+      if (rel < kMaxStagedPages) return staged[rel];
+      int blk = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t0 / p.block_size];
+      if (blk < 0 || blk >= p.num_blocks) {
+        atomicCAS(p.err, 0u, (kKernDecode << 8) | kSiteBadBlock);
+        blk = 0;
+      }
+      return blk;
+    };
+    if (LOADER && T > 0) {
+      // Whole pages in row order, one bulk copy per lane so the copies of a
+      // tile's pages are issued together; pages past the sequence (a suffix of
+      // the tile) are not fetched: the copy warps write zeros there.
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        mbar_arrive_expect_tx(&bars->q_full, kSlot);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_4d(smem + kOffQ + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64, qrow0, 0, 0);
+      }
+      const int bs = p.block_size;
+      const uint32_t page_bytes = static_cast<uint32_t>(bs) * 256;
+      int issued = 0;
+      for (int t = 0; t < 2 * T; ++t) {
+        const int slot = t % kRing;
+        const bool is_v = t != 0 && (t == 2 * T - 1 || !(t & 1));
+        const int jt = t == 0 ? 0 : (t == 2 * T - 1 ? T - 1 : ((t & 1) ? (t + 1) >> 1 : (t - 2) >> 1));
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&bars->r_empty[slot], ((t / kRing) & 1) ^ 1, abort_flag, p.err, site(1));
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        int npg = 0;
+        while (npg < kBN / bs && key0 + jt * kBN + npg * bs < kend) ++npg;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->r_stage[slot], npg * page_bytes);
+        __syncwarp();
+        if (lane < npg) {
+          const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_pages : p.k_pages);
+          const int blk = page_id(key0 + jt * kBN + lane * bs);
+          bulk_load(smem + kOffR + slot * kSlot + lane * page_bytes,
+                    base + (static_cast<int64_t>(blk) * p.Hkv + hkv) * page_bytes, page_bytes, &bars->r_stage[slot]);
+        }
+        ++issued;
+      }
+      if (lane == 0 && *abort_flag) {
+        mbar_wait_drain(&bars->q_full, 0, 200000000ull);
+        for (int t = (issued > kRing ? issued - kRing : 0); t < issued; ++t)
+          mbar_wait_drain(&bars->r_stage[t % kRing], (t / kRing) & 1, 200000000ull);
+      }
+    } else if (!LOADER && lane == 0 && T > 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
@@ -172,32 +220,7 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
         else { is_v = true; jt = (t - 2) >> 1; }
         if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
         const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
-        // Page holding key t0 (a multiple of the page size), checked.
-        auto page_id = [&](int t0) -> int {
-          const int rel = t0 / p.block_size - page0;
-          if (rel < kMaxStagedPages) return staged[rel];
-          int blk = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t0 / p.block_size];
-          if (blk < 0 || blk >= p.num_blocks) {
-            atomicCAS(p.err, 0u, (kKernDecode << 8) | kSiteBadBlock);
-            blk = 0;
-          }
-          return blk;
-        };
-        if (LOADER) {
-          // Whole pages in row order; pages past the sequence (a suffix of the
-          // tile) are not fetched: the copy warps write zeros there.
-          const int bs = p.block_size;
-          const uint32_t page_bytes = static_cast<uint32_t>(bs) * 256;
-          const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_pages : p.k_pages);
-          int npg = 0;
-          while (npg < kBN / bs && key0 + jt * kBN + npg * bs < kend) ++npg;
-          mbar_arrive_expect_tx(&bars->r_stage[slot], npg * page_bytes);
-          for (int pg = 0; pg < npg; ++pg) {
-            const int blk = page_id(key0 + jt * kBN + pg * bs);
-            bulk_load(smem + kOffR + slot * kSlot + pg * page_bytes,
-                      base + (static_cast<int64_t>(blk) * p.Hkv + hkv) * page_bytes, page_bytes, &bars->r_stage[slot]);
-          }
-        } else if (!PAGED) {
+        if (!PAGED) {
           mbar_arrive_expect_tx(&bars->r_full[slot], kSlot);
           for (int kb = 0; kb < 2; ++kb)
             tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
@@ -222,8 +245,7 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
       if (*abort_flag) {
         mbar_wait_drain(&bars->q_full, 0, 200000000ull);
         for (int t = (issued > kRing ? issued - kRing : 0); t < issued; ++t)
-          mbar_wait_drain(LOADER ? &bars->r_stage[t % kRing] : &bars->r_full[t % kRing], (t / kRing) & 1,
-                          200000000ull);
+          mbar_wait_drain(&bars->r_full[t % kRing], (t / kRing) & 1, 200000000ull);
       }
     }
   } else if (warp == 2) {
