@@ -122,29 +122,36 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     fence_barrier_init();
   }
   __syncthreads();
+  // Called by all of warp 0: lane 0 arms the stage's byte count, then every
+  // lane issues its own copies, so a paged stage's pieces go out together.
   auto issue = [&](int i) {
     const int st = i & 1;
     const int n = min(kSub, nkeys - i * kSub);
     const uint32_t bytes = static_cast<uint32_t>(n) * kRowBytes;
-    mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
+    if (lane == 0) mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
+    __syncwarp();
     if (!PAGED) {
-      bulk_load(ring + st * kStageBytes, kbase + static_cast<int64_t>(i) * kSub * kRowBytes, bytes, &sm.full[st]);
-      bulk_load(ring + st * kStageBytes + kSub * kRowBytes, vbase + static_cast<int64_t>(i) * kSub * kRowBytes,
-                bytes, &sm.full[st]);
+      if (lane == 0) {
+        bulk_load(ring + st * kStageBytes, kbase + static_cast<int64_t>(i) * kSub * kRowBytes, bytes, &sm.full[st]);
+        bulk_load(ring + st * kStageBytes + kSub * kRowBytes, vbase + static_cast<int64_t>(i) * kSub * kRowBytes,
+                  bytes, &sm.full[st]);
+      }
     } else {
-      // One copy per page piece: pages hold block_size contiguous rows of one head.
-      for (int r = 0; r < n;) {
+      // Lane r copies piece r: min(block_size, 64) rows starting at a piece
+      // boundary, which is also a page boundary or the middle of a 128-row page.
+      const int ps = min(p.block_size, kSub);
+      const int r = lane * ps;
+      if (r < n) {
         int rows;
         const uint8_t* ksrc = paged_row(p.k, p, sm.pages, page0, b, h, key0 + i * kSub + r, &rows);
         const uint8_t* vsrc = paged_row(p.v, p, sm.pages, page0, b, h, key0 + i * kSub + r, &rows);
-        rows = min(rows, n - r);
+        rows = min(min(rows, ps), n - r);
         bulk_load(ring + st * kStageBytes + r * kRowBytes, ksrc, rows * kRowBytes, &sm.full[st]);
         bulk_load(ring + st * kStageBytes + kSub * kRowBytes + r * kRowBytes, vsrc, rows * kRowBytes, &sm.full[st]);
-        r += rows;
       }
     }
   };
-  if (tid == 0) {
+  if (warp == 0) {
     if (nsub > 0) issue(0);
     if (nsub > 1) issue(1);
   }
@@ -223,8 +230,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
       }
     }
     __syncthreads();
-    if (tid == 0 && i + 2 < nsub) {
-      issue(i + 2);
+    if (i + 2 < nsub) {
+      if (warp == 0) issue(i + 2);
       ++issued;
     }
   }
