@@ -201,48 +201,52 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
         for (int t = (issued > kRing ? issued - kRing : 0); t < issued; ++t)
           mbar_wait_drain(&bars->r_stage[t % kRing], (t / kRing) & 1, 200000000ull);
       }
-    } else if (!LOADER && lane == 0 && T > 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, kSlot);
-      for (int kb = 0; kb < 2; ++kb)
-        tma_load_4d(smem + kOffQ + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64, qrow0, 0, 0);
+    } else if (!LOADER && T > 0) {
+      // TMA boxes, issued warp-wide: lane 0 waits for the slot and arms its
+      // byte count, then lane kb (contiguous cache) or lane pg (one page,
+      // both 64-column halves) issues its boxes.
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        mbar_arrive_expect_tx(&bars->q_full, kSlot);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_4d(smem + kOffQ + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64, qrow0, 0, 0);
+      }
       int issued = 0;
       for (int t = 0; t < 2 * T; ++t) {
         const int slot = t % kRing;
-        const uint32_t u = t / kRing;
-        bool is_v;
-        int jt;
-        if (t == 0) { is_v = false; jt = 0; }
-        else if (t == 2 * T - 1) { is_v = true; jt = T - 1; }
-        else if (t & 1) { is_v = false; jt = (t + 1) >> 1; }
-        else { is_v = true; jt = (t - 2) >> 1; }
-        if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        const bool is_v = t != 0 && (t == 2 * T - 1 || !(t & 1));
+        const int jt = t == 0 ? 0 : (t == 2 * T - 1 ? T - 1 : ((t & 1) ? (t + 1) >> 1 : (t - 2) >> 1));
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(&bars->r_empty[slot], ((t / kRing) & 1) ^ 1, abort_flag, p.err, site(1));
+          if (ok) mbar_arrive_expect_tx(&bars->r_full[slot], kSlot);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __syncwarp();
         const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
         if (!PAGED) {
-          mbar_arrive_expect_tx(&bars->r_full[slot], kSlot);
-          for (int kb = 0; kb < 2; ++kb)
-            tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes, tm, &bars->r_full[slot], kb * 64,
+          if (lane < 2)
+            tma_load_4d(smem + kOffR + slot * kSlot + lane * kTileBytes, tm, &bars->r_full[slot], lane * 64,
                         key0 + jt * kBN, hkv, b);
         } else {
-          mbar_arrive_expect_tx(&bars->r_full[slot], kSlot);
           const int bs = p.block_size;
-          for (int pg = 0; pg < kBN / bs; ++pg) {
-            const int t0 = key0 + jt * kBN + pg * bs;  // a multiple of bs
+          if (lane < kBN / bs) {
+            const int t0 = key0 + jt * kBN + lane * bs;  // a multiple of bs
             int blk = 0, row = 0;
             if (t0 < kend)
               blk = page_id(t0);
             else
               row = bs;  // wholly out of range: zero fill
             for (int kb = 0; kb < 2; ++kb)
-              tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes + pg * bs * 128, tm, &bars->r_full[slot],
-                          kb * 64, row, hkv, blk);
+              tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes + lane * bs * 128, tm,
+                          &bars->r_full[slot], kb * 64, row, hkv, blk);
           }
         }
         ++issued;
       }
-      if (*abort_flag) {
+      if (lane == 0 && *abort_flag) {
         mbar_wait_drain(&bars->q_full, 0, 200000000ull);
         for (int t = (issued > kRing ? issued - kRing : 0); t < issued; ++t)
           mbar_wait_drain(&bars->r_full[t % kRing], (t / kRing) & 1, 200000000ull);
