@@ -49,7 +49,7 @@ NCU_TRAFFIC = {
     "bwd_train": {"src": "5ac194ea4fb4f647", "bytes": 404825088 + 219198720},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
     # proportional to B, stored here scaled to the B=64 launch
-    "decode_split": {"src": "a53655af1af4de31", "bytes": (1073855000 + 7006208) * 8},
+    "decode_split": {"src": "e17f9f3acef4969c", "bytes": (1073865000 + 7363840) * 8},
 }
 
 
