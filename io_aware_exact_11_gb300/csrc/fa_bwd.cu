@@ -131,8 +131,9 @@ __device__ __forceinline__ bool mbar_wait_drain_inl(uint64_t* bar, uint32_t pari
 // Adds 32 columns of dQᵀ (this lane's head dim, columns cbase … cbase+31) into
 // the fp32 accumulator rows: per block of four columns, a 4 × 4 exchange among
 // lanes 4g … 4g+3 gives lane 4g + r4 column c0 + r4 for head dims 4g … 4g+3,
-// added with one 16-byte reduction.  dst points at head dim 4g of row 0.
-__device__ __forceinline__ void reduce_cols(const uint32_t (&v)[32], float* dst, int cbase, int r4) {
+// added with one 16-byte reduction (rows >= rows_valid, past N, are skipped).
+// dst points at head dim 4g of row 0.
+__device__ __forceinline__ void reduce_cols(const uint32_t (&v)[32], float* dst, int cbase, int r4, int rows_valid) {
 #pragma unroll
   for (int c0 = 0; c0 < 32; c0 += 4) {
     float a0 = __uint_as_float(v[c0]), a1 = __uint_as_float(v[c0 + 1]);
@@ -150,8 +151,9 @@ __device__ __forceinline__ void reduce_cols(const uint32_t (&v)[32], float* dst,
       if (o) { a0 = y0; a1 = y1; } else { a2 = y0; a3 = y1; }
     }
     float* q = dst + static_cast<int64_t>(cbase + c0 + r4) * kD;
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(q), "f"(a0), "f"(a1), "f"(a2), "f"(a3)
-                 : "memory");
+    if (cbase + c0 + r4 < rows_valid)
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(q), "f"(a0), "f"(a1), "f"(a2), "f"(a3)
+                   : "memory");
   }
 }
 
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int64_t bh = static_cast<int64_t>(b) * p.H + h;
-  const int T = p.N / kTile;
+  const int T = (p.N + kTile - 1) / kTile;  // the last tile may be ragged
   const int i0 = p.causal ? j : 0;  // first query tile this key tile meets
   const int nT = T - i0;            // query tiles visited; "it" counts them from 0
 
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // -------------------------------------------- Pᵀ / dSᵀ, then dK / dV out
     const int wq = warp & 3;
     const int r = wq * 32 + lane;             // key row within the tile
+    const bool key_pad = j * kTile + r >= p.N;  // past N in a ragged last key tile
     const int tr = threadIdx.x - 128;         // 0..127, for staging row stats
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
@@ -395,8 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const uint32_t ph = it & 1;
       const bool diag = p.causal && i == j;  // mask query columns c < r (key r > query c)
       named_sync(1, 128);  // every thread is done reading the previous tile's stats
-      s_lse[tr] = p.lse_log2[bh * p.N + i * kTile + tr];
-      s_del[tr] = p.delta[bh * p.N + i * kTile + tr];
+      // Query rows past N (a ragged last tile) get LSE = +∞, so their P is 0.
+      const int qrow = i * kTile + tr;
+      s_lse[tr] = qrow < p.N ? p.lse_log2[bh * p.N + qrow] : INFINITY;
+      s_del[tr] = qrow < p.N ? p.delta[bh * p.N + qrow] : 0.f;
       named_sync(1, 128);
       if (!ok) continue;
 
@@ -426,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             b0 = c + 32 < r ? 0.f : b0;
             b1 = c + 33 < r ? 0.f : b1;
           }
+          if (key_pad) a0 = a1 = b0 = b1 = 0.f;  // zero-filled K row: score 0, not −∞
           pk[half * 32 + e] = pack_bf16x2(a0, a1);
           pk[half * 32 + 16 + e] = pack_bf16x2(b0, b1);
         }
@@ -487,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           tmem_ld32(tmem + lane_base + kColDV + cc * 32, rr);
           tmem_wait_ld();
           reg_fence(rr);
-          store_row32(dv_row + cc * 32, rr, 1.f);
+          if (!key_pad) store_row32(dv_row + cc * 32, rr, 1.f);
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -495,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           tmem_ld32(tmem + lane_base + kColDK + cc * 32, rr);
           tmem_wait_ld();
           reg_fence(rr);
-          store_row32(dk_row + cc * 32, rr, p.scale);
+          if (!key_pad) store_row32(dk_row + cc * 32, rr, p.scale);
         }
       }
     }
@@ -528,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       // Column c of dQ_iᵀ is query row i·128 + c; lane 4g + r4 ends up with query
       // row c0 + r4, head dims wq·32 + 4g … +3.
       float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * kD + wq * 32 + (lane & ~3);
-      reduce_cols(r0, dst, half * 64, r4);
-      reduce_cols(r1, dst, half * 64 + 32, r4);
+      reduce_cols(r0, dst, half * 64, r4, p.N - i * kTile);
+      reduce_cols(r1, dst, half * 64 + 32, r4, p.N - i * kTile);
     }
     tc_fence_before();
     named_sync(2, kThreads);
@@ -555,7 +561,7 @@ cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t stream, int*
   cudaFuncAttributes attr;
   if ((e = cudaFuncGetAttributes(&attr, bwd_main_kernel)) != cudaSuccess) return e;
   if (attr.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
-  bwd_main_kernel<<<dim3(p.N / kTile, p.H, p.B), kThreads, kSmem, stream>>>(p);
+  bwd_main_kernel<<<dim3((p.N + kTile - 1) / kTile, p.H, p.B), kThreads, kSmem, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n4 = rows * kD / 4;

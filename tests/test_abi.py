@@ -113,7 +113,7 @@ def test_backward_rejects_bad_arguments(L):
         a.update(kw)
         return L.fa_backward(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
                              a["dt"], a["scale"], a["ws"], a["wsb"], None)
-    assert bwd(N=200) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(N=0) == fa.FA_ERR_INVALID_ARG
     assert bwd(d=64) == fa.FA_ERR_UNSUPPORTED
     assert bwd(wsb=10) == fa.FA_ERR_INVALID_ARG
     assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
@@ -132,7 +132,7 @@ def test_masked_entry_points_validate_before_cuda(L):
         return L.fa_backward_masked(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, n, 128, fa.FA_BF16,
                                     0.1, FAKE, 1 << 24, mask, None)
     assert bwdm(mask=-1) == fa.FA_ERR_INVALID_ARG
-    assert bwdm(n=200) == fa.FA_ERR_UNSUPPORTED
+    assert bwdm(n=0) == fa.FA_ERR_INVALID_ARG
 
 
 def test_gqa_decode_validates_before_cuda(L):

@@ -132,7 +132,7 @@ def _bwd(seed, B, H, N, heads=None):
         assert max(e) <= TOL_GRAD, ((b, h), e)
 
 
-@pytest.mark.parametrize("B,H,N", [(1, 2, 128), (1, 2, 256), (2, 1, 640)])
+@pytest.mark.parametrize("B,H,N", [(1, 2, 128), (1, 2, 256), (2, 1, 640), (1, 2, 300), (1, 1, 129)])
 def test_causal_backward(B, H, N):
     _bwd(25, B, H, N)
 

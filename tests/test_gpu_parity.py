@@ -239,7 +239,12 @@ def _bwd_check(seed, B, H, N, heads=None):
     return errs
 
 
-@pytest.mark.parametrize("B,H,N", [(1, 2, 128), (1, 2, 256), (2, 1, 640)])
+@pytest.mark.parametrize("B,H,N", [
+    (1, 2, 128), (1, 2, 256), (2, 1, 640),
+    (1, 2, 300),      # ragged last key and query tile
+    (2, 1, 1000),
+    (1, 3, 129),      # one key / query past a tile boundary
+])
 def test_backward_matches_oracle(B, H, N):
     _bwd_check(6, B, H, N)
 
@@ -260,9 +265,10 @@ def test_unsupported_shapes_raise_without_launching():
     with pytest.raises(fa.FAError) as ei:
         fa.forward(x, x, x)
     assert ei.value.status == fa.FA_ERR_UNSUPPORTED
-    y = torch.zeros((1, 1, 200, 128), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(fa.FAError):
+    y = torch.zeros((1, 1, 200, 64), dtype=torch.bfloat16, device="cuda")   # backward is built for d = 128
+    with pytest.raises(fa.FAError) as ei:
         fa.backward(y, y, y, y, torch.zeros((1, 1, 200), device="cuda"), y)
+    assert ei.value.status == fa.FA_ERR_UNSUPPORTED
     assert fa.launch_count() == before
 
 
