@@ -281,7 +281,7 @@ def decode_splitkv(q, k, v, n_splits: int = 32, scale: float | None = None, out=
 
 def decode_splitkv_gqa(q, k, v, n_splits: int = 32, scale: float | None = None, out=None, lse=None,
                        workspace=None, stream=None):
-    """Grouped-query split-KV decode: q [B,Hq,1,d], k/v [B,Hkv,Nkv,d], Hq = G·Hkv (G <= 8)."""
+    """Grouped-query split-KV decode: q [B,Hq,1,d], k/v [B,Hkv,Nkv,d], Hq = G·Hkv (G <= 32)."""
     torch = _torch()
     _check_cuda(q, k, v)
     B, Hq, one, d = q.shape

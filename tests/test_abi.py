@@ -140,7 +140,7 @@ def test_gqa_decode_validates_before_cuda(L):
         return L.fa_decode_splitkv_gqa(FAKE, FAKE, FAKE, FAKE, None, 2, Hq, Hkv, 300, d, fa.FA_BF16, 0.1, 32, FAKE,
                                        wsb, None)
     assert dec(Hq=28, Hkv=5) == fa.FA_ERR_INVALID_ARG          # not a multiple
-    assert dec(Hq=36, Hkv=4) == fa.FA_ERR_UNSUPPORTED          # group of 9
+    assert dec(Hq=132, Hkv=4) == fa.FA_ERR_UNSUPPORTED         # group of 33
     assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
     assert dec(wsb=64) == fa.FA_ERR_INVALID_ARG
     assert b"workspace" in L.fa_get_last_error()

@@ -50,6 +50,8 @@ def _run(seed, B, Hq, Hkv, N, splits, heads=None):
     (1, 8, 1, 2048, 32),     # one key/value head for all (group of 8)
     (2, 6, 3, 777, 7),       # group of 2, ragged split
     (1, 4, 2, 20, 32),       # more splits than keys
+    (2, 32, 2, 700, 4),      # group of 16
+    (3, 32, 1, 1500, 8),     # multi-query attention: one key/value head for 32 query heads
 ])
 def test_gqa_decode_matches_oracle(B, Hq, Hkv, N, splits):
     _run(31, B, Hq, Hkv, N, splits)

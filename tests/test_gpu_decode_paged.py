@@ -90,6 +90,8 @@ def _run(seed, B, Hq, Hkv, lens, bs, splits, heads=None):
     (2, 8, 4, [128, 1200], 128, 16),         # groups of 2, one page per tile
     (1, 8, 1, [700], 32, 1),                 # one key/value head, one split
     (1, 8, 2, [17000], 16, 1),               # 1063 pages in one split: past the 1024 staged page ids
+    (2, 32, 1, [900, 333], 16, 4),           # multi-query attention over 16-key pages
+    (2, 32, 2, [640, 129], 64, 2),           # groups of 16 over 64-key pages
 ])
 def test_paged_decode_matches_oracle(B, Hq, Hkv, lens, bs, splits):
     _run(41, B, Hq, Hkv, lens, bs, splits)
