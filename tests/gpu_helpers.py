@@ -48,3 +48,28 @@ def rel_l2(a, b) -> float:
 
 def cpu64(t) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class Guarded:
+    """A tensor of the given shape and dtype placed in the middle of a larger
+    byte buffer whose every byte starts as SENTINEL; ``intact()`` says whether
+    the GUARD bytes before and after the tensor still hold it.  GUARD is a
+    multiple of 256, so the tensor keeps the allocation's alignment."""
+
+    GUARD = 4096
+    SENTINEL = 0x5A
+
+    def __init__(self, shape, dtype, device="cuda"):
+        import torch
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.nbytes = n
+        self.raw = torch.full((self.GUARD + n + self.GUARD,), self.SENTINEL, dtype=torch.uint8, device=device)
+        self.t = self.raw[self.GUARD:self.GUARD + n].view(dtype).view(shape)
+
+    def intact(self) -> bool:
+        import torch
+        if self.raw.is_cuda:
+            torch.cuda.synchronize()
+        head = self.raw[:self.GUARD].cpu().numpy()
+        tail = self.raw[self.GUARD + self.nbytes:].cpu().numpy()
+        return bool(np.all(head == self.SENTINEL) and np.all(tail == self.SENTINEL))
