@@ -46,7 +46,7 @@ NCU_TRAFFIC = {
     # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
     "fwd_prefill": {"src": "c6c9bf8989b0aba3", "bytes": 402765568 + 119370240},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
-    "bwd_train": {"src": "5ac194ea4fb4f647", "bytes": 404825088 + 219198720},
+    "bwd_train": {"src": "e56ffe53bd1fadf6", "bytes": 404885248 + 219086336},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
     # proportional to B, stored here scaled to the B=64 launch
     "decode_split": {"src": "e17f9f3acef4969c", "bytes": (1073865000 + 7363840) * 8},
