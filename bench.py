@@ -349,7 +349,14 @@ def run_ours(args, ws, rank, local):
                                         "frac": kv_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"]),
                                         "kernel": "decode_split_kernel + decode_merge_kernel",
                                         "traffic": None if dec_traffic is None else dec_traffic * Bd / 64}}
-        del qd, kd, vd, od, ld, ws_d
+        # The same step with the library's own split choice for this shape.
+        S_auto = fa.choose_splits(Bd, Hd, Hd, Nd)
+        ws_a = torch.empty(fa.decode_workspace_size(Bd, Hd, d, S_auto), dtype=torch.uint8, device=dev)
+        t_auto = timed(lambda: fa.decode_splitkv(qd, kd, vd, n_splits=S_auto, out=od, lse=ld, workspace=ws_a),
+                       n_dec, 2) / n_dec
+        extra["decode"]["library_split_choice"] = {"splits": S_auto, "hbm_gbs": kv_bytes / t_auto / 1e9,
+                                                   "tokens_per_s": Bd / t_auto, "ms": t_auto * 1e3}
+        del qd, kd, vd, od, ld, ws_d, ws_a
 
     if "gqa" in extras:
         # ---------------- grouped-query decode, the lab model's 28 query / 4 key-value heads

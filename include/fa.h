@@ -146,6 +146,17 @@ FA_API fa_status fa_forward_host(const void* q, const void* k, const void* v, vo
                                  void* stream);
 
 /*
+ * fa_decode_choose_splits — a split count for the decode entry points that keeps
+ *   the GPU busy without making chunks too short: about 27 CTAs per SM for
+ *   single-head decode (three are resident per SM), about one per SM for
+ *   grouped decode (H_q > H_kv, one resident per SM), at least 256 keys per
+ *   split, rounded to a power of two and clamped to [1, 256].  Fitted to
+ *   measurements on GB300; uses the current device's SM count (152 if none can
+ *   be queried).  Returns 0 for non-positive sizes or H_q not a multiple of H_kv.
+ */
+FA_API int fa_decode_choose_splits(int B, int H_q, int H_kv, int N_kv);
+
+/*
  * fa_decode_workspace_size — bytes of workspace fa_decode_splitkv needs:
  *   the partial outputs B·H·n_splits·d·4 bytes and the partial (m, ℓ) pairs
  *   B·H·n_splits·2·4 bytes, each rounded up to a multiple of 256.

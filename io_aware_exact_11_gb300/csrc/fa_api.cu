@@ -459,6 +459,23 @@ fa_status fa_forward_host(const void* q, const void* k, const void* v, void* o, 
   return ok();
 }
 
+int fa_decode_choose_splits(int B, int H_q, int H_kv, int N_kv) {
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || N_kv <= 0 || H_q % H_kv != 0) return 0;
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 152;
+  cudaGetLastError();  // a failed query on a machine without a device is not an error here
+  const bool grouped = H_q > H_kv;
+  const double heads = static_cast<double>(B) * (grouped ? H_kv : H_q);
+  const double want = (grouped ? 1.0 : 27.0) * sms / heads;  // splits that give the target CTA count
+  int s = 1;
+  while (s < 256 && 2.0 * s <= want * 1.41421356) s *= 2;  // nearest power of two (geometric)
+  while (s > 1 && static_cast<int64_t>(s) * 256 > N_kv) s /= 2;
+  return s;
+}
+
 size_t fa_decode_workspace_size(int B, int H, int d, int n_splits) {
   if (B <= 0 || H <= 0 || d <= 0 || n_splits <= 0) return 0;
   const size_t slots = static_cast<size_t>(B) * H * n_splits;

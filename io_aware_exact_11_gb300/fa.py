@@ -27,6 +27,7 @@ EXPORTED = (
     "fa_forward_fp8",
     "fa_forward_host_workspace_size",
     "fa_forward_host",
+    "fa_decode_choose_splits",
     "fa_decode_workspace_size",
     "fa_decode_splitkv",
     "fa_decode_splitkv_gqa",
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.fa_forward_host_workspace_size.restype = sz
         L.fa_forward_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, sz, vp]
         L.fa_forward_host.restype = i32
+        L.fa_decode_choose_splits.argtypes = [i32, i32, i32, i32]
+        L.fa_decode_choose_splits.restype = i32
         L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fa_decode_workspace_size.restype = sz
         L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
@@ -252,9 +255,18 @@ def decode_workspace_size(B: int, H: int, d: int, n_splits: int) -> int:
     return int(lib().fa_decode_workspace_size(B, H, d, n_splits))
 
 
-def decode_splitkv(q, k, v, n_splits: int = 32, scale: float | None = None, out=None, lse=None,
+def choose_splits(B: int, Hq: int, Hkv: int, Nkv: int) -> int:
+    """The library's split count for a decode shape (fa_decode_choose_splits)."""
+    s = int(lib().fa_decode_choose_splits(B, Hq, Hkv, Nkv))
+    if s <= 0:
+        raise FAError(FA_ERR_INVALID_ARG, f"no split count for B={B} Hq={Hq} Hkv={Hkv} Nkv={Nkv}")
+    return s
+
+
+def decode_splitkv(q, k, v, n_splits: int | None = None, scale: float | None = None, out=None, lse=None,
                    workspace=None, stream=None):
-    """Split-KV decode: q [B,H,1,d] against k/v [B,H,Nkv,d]; returns (O, LSE)."""
+    """Split-KV decode: q [B,H,1,d] against k/v [B,H,Nkv,d]; returns (O, LSE).
+    n_splits=None takes the library's choice for the shape."""
     torch = _torch()
     _check_cuda(q, k, v)
     B, H, one, d = q.shape
@@ -264,6 +276,8 @@ def decode_splitkv(q, k, v, n_splits: int = 32, scale: float | None = None, out=
     for t in (q, k, v):
         if not t.is_contiguous():
             raise ValueError("decode inputs must be contiguous")
+    if n_splits is None:
+        n_splits = choose_splits(B, H, H, Nkv)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -279,9 +293,10 @@ def decode_splitkv(q, k, v, n_splits: int = 32, scale: float | None = None, out=
     return out, lse
 
 
-def decode_splitkv_gqa(q, k, v, n_splits: int = 32, scale: float | None = None, out=None, lse=None,
+def decode_splitkv_gqa(q, k, v, n_splits: int | None = None, scale: float | None = None, out=None, lse=None,
                        workspace=None, stream=None):
-    """Grouped-query split-KV decode: q [B,Hq,1,d], k/v [B,Hkv,Nkv,d], Hq = G·Hkv (G <= 32)."""
+    """Grouped-query split-KV decode: q [B,Hq,1,d], k/v [B,Hkv,Nkv,d], Hq = G·Hkv (G <= 32).
+    n_splits=None takes the library's choice for the shape."""
     torch = _torch()
     _check_cuda(q, k, v)
     B, Hq, one, d = q.shape
@@ -291,6 +306,8 @@ def decode_splitkv_gqa(q, k, v, n_splits: int = 32, scale: float | None = None, 
     for t in (q, k, v):
         if not t.is_contiguous():
             raise ValueError("decode inputs must be contiguous")
+    if n_splits is None:
+        n_splits = choose_splits(B, Hq, Hkv, Nkv)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -306,12 +323,13 @@ def decode_splitkv_gqa(q, k, v, n_splits: int = 32, scale: float | None = None, 
     return out, lse
 
 
-def decode_paged(q, k_cache, v_cache, block_table, seq_lens, n_splits: int = 8, scale: float | None = None,
-                 out=None, lse=None, workspace=None, stream=None):
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, n_splits: int | None = None,
+                 scale: float | None = None, out=None, lse=None, workspace=None, stream=None):
     """Split-KV decode over a paged cache.
 
     q [B,Hq,1,d]; k_cache/v_cache [num_blocks, Hkv, block_size, d]; block_table
-    [B, max_blocks] int32; seq_lens [B] int32 (device tensors).
+    [B, max_blocks] int32; seq_lens [B] int32 (device tensors).  n_splits=None
+    takes the library's choice for the longest sequence the table can hold.
     """
     torch = _torch()
     _check_cuda(q, k_cache, v_cache, block_table, seq_lens)
@@ -324,6 +342,8 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, n_splits: int = 8, 
     for t in (q, k_cache, v_cache, block_table, seq_lens):
         if not t.is_contiguous():
             raise ValueError("paged decode inputs must be contiguous")
+    if n_splits is None:
+        n_splits = choose_splits(B, Hq, Hkv, block_table.shape[1] * bs)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:

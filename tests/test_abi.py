@@ -188,3 +188,20 @@ def test_host_forward_validates_before_cuda(L):
     need = L.fa_forward_host_workspace_size(2, 3, 128, 128, 128, fa.FA_BF16, 2)
     assert fh(wsb=need - 1) == fa.FA_ERR_INVALID_ARG
     assert b"workspace" in L.fa_get_last_error()
+
+
+def test_decode_split_choice(L):
+    # No device here: the choice is made for 152 SMs.  Single-head decode aims at
+    # ~27 CTAs per SM, grouped decode at ~1, with at least 256 keys per split.
+    assert L.fa_decode_choose_splits(1, 32, 32, 8192) == 32      # capped by 8192 / 256 keys
+    assert L.fa_decode_choose_splits(4, 32, 32, 8192) == 32
+    assert L.fa_decode_choose_splits(64, 32, 32, 8192) == 2
+    assert L.fa_decode_choose_splits(1, 28, 4, 32768) == 32
+    assert L.fa_decode_choose_splits(8, 28, 4, 8192) == 4
+    assert L.fa_decode_choose_splits(64, 28, 4, 8192) == 1
+    assert L.fa_decode_choose_splits(1, 32, 32, 100) == 1         # a short sequence is not split
+    assert L.fa_decode_choose_splits(0, 32, 32, 8192) == 0
+    assert L.fa_decode_choose_splits(1, 30, 4, 8192) == 0         # H_q not a multiple of H_kv
+    for B, Hq, Hkv, N in ((1, 1, 1, 1 << 20), (3, 64, 8, 5000)):
+        s = L.fa_decode_choose_splits(B, Hq, Hkv, N)
+        assert 1 <= s <= 256 and s & (s - 1) == 0
