@@ -269,7 +269,7 @@ FA_API size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *   q, k, v, o, dout, dq, dk, dv: [B,H,N,d] contiguous; lse [B,H,N] float32 as
  *   written by fa_forward.  workspace: at least fa_backward_workspace_size()
  *   bytes; the library clears what it needs cleared.
- *   Supported: FA_BF16, d = 128, any N >= 1 (a ragged last tile is masked).
+ *   Supported: FA_BF16, d = 64 or 128, any N >= 1 (a ragged last tile is masked).
  */
 FA_API fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,

@@ -761,7 +761,8 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
     return fail(FA_ERR_INVALID_ARG, "fa_backward: null pointer");
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return fail(FA_ERR_INVALID_ARG, "fa_backward: sizes must be positive");
   if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_backward: unknown dtype");
-  if (dtype != FA_BF16 || d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_backward: only bf16 with d=128 is built");
+  if (dtype != FA_BF16 || (d != 64 && d != 128))
+    return fail(FA_ERR_UNSUPPORTED, "fa_backward: only bf16 with d = 64 or 128 is built");
   if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_backward: B and H must be <= 65535");
   if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_backward: scale must be finite and > 0");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||

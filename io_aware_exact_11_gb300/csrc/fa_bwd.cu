@@ -45,7 +45,7 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 128;
+constexpr int kD = 128;  // layout width: shared-memory tiles and TMEM columns are sized for d = 128
 constexpr int kTile = 128;
 constexpr int kTileBytes = 128 * 128;   // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kOpBytes = 2 * kTileBytes;  // one 128 × 128 bf16 operand
@@ -132,7 +132,8 @@ __device__ __forceinline__ bool mbar_wait_drain_inl(uint64_t* bar, uint32_t pari
 // the fp32 accumulator rows: per block of four columns, a 4 × 4 exchange among
 // lanes 4g … 4g+3 gives lane 4g + r4 column c0 + r4 for head dims 4g … 4g+3,
 // added with one 16-byte reduction (rows >= rows_valid, past N, are skipped).
-// dst points at head dim 4g of row 0.
+// dst points at head dim 4g of row 0; rows are D floats apart.
+template <int D>
 __device__ __forceinline__ void reduce_cols(const uint32_t (&v)[32], float* dst, int cbase, int r4, int rows_valid) {
 #pragma unroll
   for (int c0 = 0; c0 < 32; c0 += 4) {
@@ -150,7 +151,7 @@ __device__ __forceinline__ void reduce_cols(const uint32_t (&v)[32], float* dst,
       const float y1 = __shfl_xor_sync(0xffffffffu, o ? a1 : a3, 2);
       if (o) { a0 = y0; a1 = y1; } else { a2 = y0; a3 = y1; }
     }
-    float* q = dst + static_cast<int64_t>(cbase + c0 + r4) * kD;
+    float* q = dst + static_cast<int64_t>(cbase + c0 + r4) * D;
     if (cbase + c0 + r4 < rows_valid)
       asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(q), "f"(a0), "f"(a1), "f"(a2), "f"(a3)
                    : "memory");
@@ -158,16 +159,19 @@ __device__ __forceinline__ void reduce_cols(const uint32_t (&v)[32], float* dst,
 }
 
 // ---------------------------------------------------------------- kernel 1
-// D_i = Σ_t dO_it O_it and LSE·log2(e), one half-warp per row.
+// D_i = Σ_t dO_it O_it and LSE·log2(e), D/8 lanes per row (8 bf16 each).
+template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+  constexpr int kLanes = D / 8;           // lanes per row
+  constexpr int kRowsPerWarp = 32 / kLanes;
   const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.N;
-  const int half = (threadIdx.x & 31) >> 4;
-  const int l16 = threadIdx.x & 15;
+  const int sub = (threadIdx.x & 31) / kLanes;
+  const int l16 = threadIdx.x % kLanes;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t r = gw * 2 + half; r < rows; r += nw * 2) {
-    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.o) + r * kD * 2 + l16 * 16);
-    const uint4 g = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.dout) + r * kD * 2 + l16 * 16);
+  for (int64_t r = gw * kRowsPerWarp + sub; r < rows; r += nw * kRowsPerWarp) {
+    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.o) + r * D * 2 + l16 * 16);
+    const uint4 g = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.dout) + r * D * 2 + l16 * 16);
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
     const uint32_t wg[4] = {g.x, g.y, g.z, g.w};
     float acc = 0.f;
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
       acc = fmaf(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(wg[i] & 0xFFFF0000u), acc);
     }
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (l16 == 0) {
       p.delta[r] = acc;
       p.lse_log2[r] = p.lse[r] * 1.4426950408889634f;
@@ -186,8 +190,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
 }
 
 // ---------------------------------------------------------------- kernel 3
+template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BwdParams p) {
-  const int64_t n4 = static_cast<int64_t>(p.B) * p.H * p.N * kD / 4;
+  const int64_t n4 = static_cast<int64_t>(p.B) * p.H * p.N * D / 4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(p.dq_acc)[i];
@@ -215,7 +220,9 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------- kernel 2
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  constexpr int kNKB = D / 64;  // 64-column blocks a Q, K, V or dO tile fills
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 256);
+    mbar_init(&bars->dq_free, 2 * D);  // the drain warps that own head dims < D
     mbar_init(&bars->p_ready, 128);
     mbar_init(&bars->ds_ready, 128);
     mbar_init(&bars->ds_free, 1);
@@ -251,6 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
+  }
+  if constexpr (D < kD) {
+    // K's head dims D..127 are never loaded; the dQᵀ MMA reads them as rows of
+    // its M = 128 operand, so they must be zeros.
+    for (int o = threadIdx.x * 16; o < (kD - D) / 64 * kTileBytes; o += kThreads * 16)
+      *reinterpret_cast<uint4*>(smem + kOffK + kNKB * kTileBytes + o) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -273,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * kOpBytes);
-      for (int kb = 0; kb < 2; ++kb) {
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * kNKB * kTileBytes);
+      for (int kb = 0; kb < kNKB; ++kb) {
         tma_load_4d(smem + kOffK + kb * kTileBytes, &p.tm_k, &bars->kv_full, kb * 64, j * kTile, h, b);
         tma_load_4d(smem + kOffV + kb * kTileBytes, &p.tm_v, &bars->kv_full, kb * 64, j * kTile, h, b);
       }
@@ -283,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         const int i = i0 + it;
         const int qb = it & 1;
         if (!mbar_wait_inl(&bars->q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.err, site(1))) break;
-        mbar_arrive_expect_tx(&bars->q_full[qb], 2 * kOpBytes);
-        for (int kb = 0; kb < 2; ++kb) {
+        mbar_arrive_expect_tx(&bars->q_full[qb], 2 * kNKB * kTileBytes);
+        for (int kb = 0; kb < kNKB; ++kb) {
           tma_load_4d(smem + kOffQ + qb * kOpBytes + kb * kTileBytes, &p.tm_q, &bars->q_full[qb], kb * 64,
                       i * kTile, h, b);
           tma_load_4d(smem + kOffDO + qb * kOpBytes + kb * kTileBytes, &p.tm_do, &bars->q_full[qb], kb * 64,
@@ -302,15 +316,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // Sᵀ, dPᵀ
-      constexpr uint32_t kIdescKM = idesc_bf16_f32(128, kD, false, true);    // dV (A in TMEM), dK
-      constexpr uint32_t kIdescMM = idesc_bf16_f32(128, kD, true, true);     // dQ
+      constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV (A in TMEM), dK
+      // dQᵀ keeps M = 128 for every D: with D = 64 its A operand (K read MN-major)
+      // covers a zeroed second 64-column block, so TMEM lanes 64..127 hold zeros.
+      constexpr uint32_t kIdescMM = idesc_bf16_f32(128, kTile, true, true);  // dQᵀ
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sQ = smem_u32(smem + kOffQ), sDO = smem_u32(smem + kOffDO);
       const uint32_t sDST = smem_u32(smem + kOffDST);
       auto issue_st = [&](int it) {  // Sᵀ = K_j Q_iᵀ for the it-th visited query tile
         const uint32_t q = sQ + (it & 1) * kOpBytes;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
           mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024), kIdescKK,
                       kk > 0 ? 1u : 0u);
@@ -331,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         if (!(ok = mbar_wait_inl(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(4)))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
           mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), kIdescKK,
                       kk > 0 ? 1u : 0u);
@@ -485,10 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         const int64_t grow = bh * p.N + static_cast<int64_t>(j) * kTile + r;
-        __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + grow * kD;
-        __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + grow * kD;
+        __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + grow * D;
+        __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + grow * D;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t rr[32];
           tmem_ld32(tmem + lane_base + kColDV + cc * 32, rr);
           tmem_wait_ld();
@@ -496,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           if (!key_pad) store_row32(dv_row + cc * 32, rr, 1.f);
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t rr[32];
           tmem_ld32(tmem + lane_base + kColDK + cc * 32, rr);
           tmem_wait_ld();
@@ -514,11 +530,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     // exchange among neighbouring lanes turns "lane = head-dim index" into four
     // consecutive head dims of one query row per lane, so every reduction
     // instruction adds 16 bytes per lane: four full 128-byte lines per warp.
+    // TMEM lane = head dim, so with D < 128 the warps of lane quarters at or
+    // past D have nothing to drain (they hold the zero rows) and sit this out.
     const int half = (warp - 8) >> 2;
     const int wq = warp & 3;
     const int r4 = lane & 3;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    for (int it = 0; it < nT; ++it) {
+    for (int it = 0; wq * 32 < D && it < nT; ++it) {
       const int i = i0 + it;
       const bool ok = mbar_wait_inl(&bars->dq_full, it & 1, abort_flag, p.err, site(12));
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -533,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       mbar_arrive(&bars->dq_free);
       // Column c of dQ_iᵀ is query row i·128 + c; lane 4g + r4 ends up with query
       // row c0 + r4, head dims wq·32 + 4g … +3.
-      float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * kD + wq * 32 + (lane & ~3);
-      reduce_cols(r0, dst, half * 64, r4, p.N - i * kTile);
-      reduce_cols(r1, dst, half * 64 + 32, r4, p.N - i * kTile);
+      float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * D + wq * 32 + (lane & ~3);
+      reduce_cols<D>(r0, dst, half * 64, r4, p.N - i * kTile);
+      reduce_cols<D>(r1, dst, half * 64 + 32, r4, p.N - i * kTile);
     }
     tc_fence_before();
     named_sync(2, kThreads);
@@ -544,31 +562,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 
 }  // namespace
 
-cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t stream, int* launches) {
-  *launches = 0;
-  if (d != kD) return cudaErrorInvalidValue;
+namespace {
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, int* launches) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.N;
-  cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * kD * sizeof(float), stream);
+  cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   const int pre_blocks = static_cast<int>(std::min<int64_t>((rows + 15) / 16, 152 * 16));
-  bwd_preprocess_kernel<<<pre_blocks, 256, 0, stream>>>(p);
+  bwd_preprocess_kernel<D><<<pre_blocks, 256, 0, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
+      cudaSuccess)
     return e;
   // setmaxnreg.inc waits until the block's pool can supply the registers: refuse
   // to launch unless ptxas gave the kernel the count the split assumes.
   cudaFuncAttributes attr;
-  if ((e = cudaFuncGetAttributes(&attr, bwd_main_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&attr, bwd_main_kernel<D>)) != cudaSuccess) return e;
   if (attr.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
-  bwd_main_kernel<<<dim3((p.N + kTile - 1) / kTile, p.H, p.B), kThreads, kSmem, stream>>>(p);
+  bwd_main_kernel<D><<<dim3((p.N + kTile - 1) / kTile, p.H, p.B), kThreads, kSmem, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t n4 = rows * kD / 4;
+  const int64_t n4 = rows * D / 4;
   const int cv_blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 152 * 8));
-  bwd_dq_convert_kernel<<<cv_blocks, 256, 0, stream>>>(p);
+  bwd_dq_convert_kernel<D><<<cv_blocks, 256, 0, stream>>>(p);
   ++*launches;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t stream, int* launches) {
+  *launches = 0;
+  if (d == 128) return launch_bwd_d<128>(p, stream, launches);
+  if (d == 64) return launch_bwd_d<64>(p, stream, launches);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

@@ -114,7 +114,8 @@ def test_backward_rejects_bad_arguments(L):
         return L.fa_backward(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
                              a["dt"], a["scale"], a["ws"], a["wsb"], None)
     assert bwd(N=0) == fa.FA_ERR_INVALID_ARG
-    assert bwd(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(dt=fa.FA_FP32) == fa.FA_ERR_UNSUPPORTED
     assert bwd(wsb=10) == fa.FA_ERR_INVALID_ARG
     assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert bwd(ws=None) == fa.FA_ERR_INVALID_ARG

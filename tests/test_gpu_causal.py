@@ -118,8 +118,7 @@ def test_causal_prefill_full_size_sampled():
         assert max_abs(cpu64(lse[b, h])[rows], rl) <= TOL_LSE_BF16
 
 
-def _bwd(seed, B, H, N, heads=None):
-    d = 128
+def _bwd(seed, B, H, N, heads=None, d=128):
     host, dev = make_qkv(seed, B, H, N, N, d, "bf16", with_do=True)
     scale = 1 / math.sqrt(d)
     o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale, causal=True)
@@ -135,6 +134,11 @@ def _bwd(seed, B, H, N, heads=None):
 @pytest.mark.parametrize("B,H,N", [(1, 2, 128), (1, 2, 256), (2, 1, 640), (1, 2, 300), (1, 1, 129)])
 def test_causal_backward(B, H, N):
     _bwd(25, B, H, N)
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 2, 384), (1, 1, 300)])
+def test_causal_backward_head_dim_64(B, H, N):
+    _bwd(27, B, H, N, d=64)
 
 
 @pytest.mark.slow

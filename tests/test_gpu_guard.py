@@ -66,14 +66,14 @@ def test_fp8_and_fp32_forward_writes_stay_inside():
     _check(o32, l32)
 
 
-@pytest.mark.parametrize("B,H,N", [(1, 2, 300), (2, 1, 129)])
+@pytest.mark.parametrize("B,H,N,d", [(1, 2, 300, 128), (2, 1, 129, 128), (1, 3, 200, 64)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_backward_writes_stay_inside_gradients_and_workspace(B, H, N, causal):
+def test_backward_writes_stay_inside_gradients_and_workspace(B, H, N, d, causal):
     import torch
-    _, dev = make_qkv(63, B, H, N, N, 128, "bf16", with_do=True)
+    _, dev = make_qkv(63, B, H, N, N, d, "bf16", with_do=True)
     o, lse = fa.forward(dev["q"], dev["k"], dev["v"], causal=causal)
-    grads = [Guarded((B, H, N, 128), torch.bfloat16) for _ in range(3)]
-    ws = Guarded((int(fa.lib().fa_backward_workspace_size(B, H, N, 128)),), torch.uint8)
+    grads = [Guarded((B, H, N, d), torch.bfloat16) for _ in range(3)]
+    ws = Guarded((int(fa.lib().fa_backward_workspace_size(B, H, N, d)),), torch.uint8)
     fa.backward(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], dq=grads[0].t, dk=grads[1].t, dv=grads[2].t,
                 workspace=ws.t, causal=causal)
     _check(*grads, ws)

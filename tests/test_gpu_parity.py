@@ -221,8 +221,7 @@ def test_decode_full_size_sampled():
 # --------------------------------------------------------------- backward
 
 
-def _bwd_check(seed, B, H, N, heads=None):
-    d = 128
+def _bwd_check(seed, B, H, N, heads=None, d=128):
     host, dev = make_qkv(seed, B, H, N, N, d, "bf16", with_do=True)
     scale = 1 / math.sqrt(d)
     o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale)
@@ -249,6 +248,38 @@ def test_backward_matches_oracle(B, H, N):
     _bwd_check(6, B, H, N)
 
 
+@pytest.mark.parametrize("B,H,N", [(1, 2, 256), (1, 2, 300), (2, 1, 129)])
+def test_backward_head_dim_64_matches_oracle(B, H, N):
+    """d = 64: K's unused head-dim block is zeroed in shared memory so dQᵀ keeps
+    its 128-row MMA; only the drain warps of head dims 0..63 reduce."""
+    _bwd_check(7, B, H, N, d=64)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_single_key_degenerate(d):
+    """N = 1: P = 1, so O = V, D = dO·V = dP and dS = P∘(dP − D) = 0 exactly;
+    the exact dQ and dK are zero and dV = dO.  The kernel forms dP with the MMA
+    and D with a separate fp32 sum of the same exact bf16 products, so dP − D
+    is only summation-order rounding: at most d additions per side, each off by
+    ≤ 2⁻²⁴ of the running magnitude (2⁻²³ allowed for the tensor core, whose
+    accumulator may truncate), so |dP − D| ≤ 3·d·2⁻²⁴·Σ_t|dO_t V_t|.  Then
+    |dQ_t| ≤ σ·|dS|·|K_t| (and |dK_t| likewise with Q_t) up to two bf16 roundings."""
+    import torch
+    B, H, N = 2, 3, 1
+    host, dev = make_qkv(8, B, H, N, N, d, "bf16", with_do=True)
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale)
+    dq, dk, dv = fa.backward(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], scale)
+    fa.device_status()
+    assert torch.equal(dv, dev["do"])
+    for b in range(B):
+        for h in range(H):
+            q, k, v, do = (f64(host[n][b, h], "bf16")[0] for n in ("q", "k", "v", "do"))
+            gamma = 3 * d * 2.0 ** -24 * float(np.abs(do * v).sum())
+            assert float(np.abs(cpu64(dq[b, h])).max()) <= 1.01 * scale * gamma * float(np.abs(k).max())
+            assert float(np.abs(cpu64(dk[b, h])).max()) <= 1.01 * scale * gamma * float(np.abs(q).max())
+
+
 @pytest.mark.slow
 def test_backward_train_full_size_sampled():
     """B=2, H=16, N=8192, d=128: two whole heads against the oracle."""
@@ -265,7 +296,7 @@ def test_unsupported_shapes_raise_without_launching():
     with pytest.raises(fa.FAError) as ei:
         fa.forward(x, x, x)
     assert ei.value.status == fa.FA_ERR_UNSUPPORTED
-    y = torch.zeros((1, 1, 200, 64), dtype=torch.bfloat16, device="cuda")   # backward is built for d = 128
+    y = torch.zeros((1, 1, 200, 128), dtype=torch.float32, device="cuda")   # backward is built for bf16 only
     with pytest.raises(fa.FAError) as ei:
         fa.backward(y, y, y, y, torch.zeros((1, 1, 200), device="cuda"), y)
     assert ei.value.status == fa.FA_ERR_UNSUPPORTED

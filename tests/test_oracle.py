@@ -254,6 +254,21 @@ def test_backward_delta_identity():
     assert np.allclose(np.sum(p * dp, axis=1), oracle.backward_delta(do, o), atol=1e-13)
 
 
+def test_backward_single_key_closed_form():
+    """One key: every query's softmax row is [1], so O = V, dV = Σ_i dO_i and
+    dS = P∘(dP − D) vanishes, leaving dQ = dK = 0."""
+    q = RNG.standard_normal((5, 4))
+    k = RNG.standard_normal((1, 4))
+    v = RNG.standard_normal((1, 4))
+    do = RNG.standard_normal((5, 4))
+    o, lse = oracle.attention_forward(q, k, v, 0.5)
+    assert np.allclose(o, np.repeat(v, 5, axis=0), atol=1e-15)
+    assert np.allclose(lse, 0.5 * (q @ k[0]), atol=1e-14)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.5)
+    assert np.abs(dq).max() <= 1e-14 and np.abs(dk).max() <= 1e-14
+    assert np.allclose(dv, do.sum(axis=0, keepdims=True), atol=1e-14)
+
+
 def test_backward_matches_torch_autograd_fp64():
     torch = pytest.importorskip("torch")
     q = RNG.standard_normal((2, 3, 17, 8))
