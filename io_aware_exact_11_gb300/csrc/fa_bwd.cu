@@ -85,49 +85,6 @@ static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernBwd << 8) | s; }
 
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void reg_alloc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-// Bounded mbarrier wait with the polling loop inlined: warps whose register
-// limit was lowered cannot call the out-of-line slow path.
-__device__ __forceinline__ bool mbar_wait_inl(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              unsigned int* err, unsigned int code) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 31u) == 0u) {
-      if (*abort_flag) return false;
-      if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) {
-        *abort_flag = 1;
-        return false;
-      }
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-        atomicCAS(err, 0u, code);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-__device__ __forceinline__ bool mbar_wait_drain_inl(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) return false;
-  }
-  return true;
-}
-
 // Adds 32 columns of dQᵀ (this lane's head dim, columns cbase … cbase+31) into
 // the fp32 accumulator rows: per block of four columns, a 4 × 4 exchange among
 // lanes 4g … 4g+3 gives lane 4g + r4 column c0 + r4 for head dims 4g … 4g+3,

@@ -107,8 +107,30 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// Barrier waits with the polling loop inlined or out of line.  Which one gives
+// the better code differs by instantiation (measured on GB300: inlined waits
+// cost bf16 d = 128 about 5 % and gain 5 % at E4M3 and 8 % at d = 64).
+template <int D, bool FP8>
+struct FwdWait {
+  static constexpr bool kInline = FP8 || D == 64;
+  __device__ static __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned int* err, unsigned int code) {
+    if constexpr (kInline)
+      return mbar_wait_inl(bar, parity, abort_flag, err, code);
+    else
+      return mbar_wait(bar, parity, abort_flag, err, code);
+  }
+  __device__ static __forceinline__ bool drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+    if constexpr (kInline)
+      return mbar_wait_drain_inl(bar, parity, timeout_ns);
+    else
+      return mbar_wait_drain(bar, parity, timeout_ns);
+  }
+};
+
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
+  using W = FwdWait<D, FP8>;
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -165,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       for (int t = 0; t < 2 * T; ++t) {
         const int slot = t % L::kRing;
         const uint32_t u = t / L::kRing;
-        if (!mbar_wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        if (!W::wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
         mbar_arrive_expect_tx(&bars->r_full[slot], L::kSlot);
         const CUtensorMap* tm = (t & 1) ? &p.tm_v : &p.tm_k;
         for (int kb = 0; kb < L::kNKB; ++kb)
@@ -174,9 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         ++issued;
       }
       if (*abort_flag) {
-        mbar_wait_drain(&bars->q_full, 0, 200000000ull);
+        W::drain(&bars->q_full, 0, 200000000ull);
         for (int t = (issued > L::kRing ? issued - L::kRing : 0); t < issued; ++t)
-          mbar_wait_drain(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, 200000000ull);
+          W::drain(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, 200000000ull);
       }
     }
   } else if (warp == 1) {
@@ -187,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       const uint32_t sQ = smem_u32(smem + L::kQ);
       const uint32_t sR = smem_u32(smem + L::kR);
       auto ring_wait = [&](int t, unsigned int where) -> bool {
-        return mbar_wait(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, abort_flag, p.err, site(where));
+        return W::wait(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, abort_flag, p.err, site(where));
       };
       auto issue_s = [&](int i, uint32_t kb) {  // S_i = Q_i K_jᵀ
         const uint32_t qb = sQ + i * L::kSlot;
@@ -201,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             mma_bf16_ss(tmem + i * kBN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, site(5)) && ring_wait(0, 6);
+      bool ok = W::wait(&bars->q_full, 0, abort_flag, p.err, site(5)) && ring_wait(0, 6);
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < kQT; ++i) {
@@ -216,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         const bool next = j + 1 < T;
         const uint32_t kb = sR + ((tv + 1) % L::kRing) * L::kSlot;
         for (int i = 0; i < kQT && ok; ++i) {
-          if (!(ok = mbar_wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
+          if (!(ok = W::wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
           if (i == 0 && next && !(ok = ring_wait(tv + 1, 6))) break;
           tc_fence_after();
           // O_i += P̃_i V_j: A = P̃_i from S_i's TMEM columns (32 bytes of keys = 8
@@ -236,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       }
       if (*abort_flag) {
         mma_commit(&bars->drain);
-        mbar_wait_drain(&bars->drain, 0, 200000000ull);
+        W::drain(&bars->drain, 0, 200000000ull);
       }
     }
   } else {
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(&bars->s_full[qt], j & 1, abort_flag, p.err, site(8));
+      ok = W::wait(&bars->s_full[qt], j & 1, abort_flag, p.err, site(8));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       // S_1(j) is complete, so K_j and V_{j−1} have been read by both tiles.
       if (releaser) {
@@ -361,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       m_run = m_new;
     }
     if (ok) {
-      ok = mbar_wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
+      ok = W::wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         const float inv = p.o_scale / l_run;

@@ -313,6 +313,52 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, 
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+// Register split between warpgroups (setmaxnreg): every thread of a warpgroup
+// executes the same one.  An increase waits until the block's pool (threads ×
+// registers at launch) can supply it, so the splits must add up within it.
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Bounded mbarrier wait with the polling loop inlined: warps whose register
+// limit was lowered cannot call the out-of-line slow path.
+__device__ __forceinline__ bool mbar_wait_inl(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned int* err, unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        atomicCAS(err, 0u, code);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_drain_inl(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+// Named barrier `id` (1..15) over the first n threads that reach it (n a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 // Maximum of three values in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
