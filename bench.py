@@ -44,12 +44,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
-    "fwd_prefill": {"src": "c6c9bf8989b0aba3", "bytes": 402765568 + 119370240},
+    "fwd_prefill": {"src": "ae5ff0df3d5a5b5f", "bytes": 402714368 + 119067136},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
-    "bwd_train": {"src": "e56ffe53bd1fadf6", "bytes": 404885248 + 219086336},
+    "bwd_train": {"src": "385b27ebb998cd6d", "bytes": 405303040 + 219291392},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
     # proportional to B, stored here scaled to the B=64 launch
-    "decode_split": {"src": "e17f9f3acef4969c", "bytes": (1073865000 + 7363840) * 8},
+    "decode_split": {"src": "8261e7e17c87db05", "bytes": (1073901568 + 6750464) * 8},
 }
 
 
