@@ -25,8 +25,7 @@
 // 4 × 4 exchange among neighbouring lanes then gives each lane four consecutive
 // head dims of one query row, and every 16-byte-per-lane reduction covers four
 // full 128-byte lines.  Those reductions (as many bytes as the whole fp32 dQ
-// once per key tile) are what the L2 has to absorb, so two warpgroups issue
-// them, each for half of the query columns.
+// once per key tile) are what the L2 has to absorb.
 //
 // Causal mask (query i sees key j when j <= i): key tile j only meets query
 // tiles i >= j, so the loop starts at its diagonal tile, where Pᵀ entries with
@@ -34,10 +33,10 @@
 //
 // Warp roles (512 threads, four warpgroups, registers rebalanced with
 // setmaxnreg): warp 0 TMA producer and warp 1 TMEM owner + MMA issuer (warps 2,
-// 3 idle); warps 4..7 compute Pᵀ and dSᵀ (thread = key row) and write dK/dV at
-// the end; warps 8..11 and 12..15 drain dQ_iᵀ columns 0..63 and 64..127 from
-// TMEM (thread = head-dim index) into the accumulator.
-// TMEM columns: Sᵀ (then Pᵀ in 0..63) 0..127, dPᵀ (then dQ_iᵀ) 128..255,
+// 3 idle); warps 4..7 and 8..11 compute Pᵀ and dSᵀ (thread = key row) for query
+// columns 0..63 and 64..127 and write dV and dK at the end; warps 12..15 drain
+// dQ_iᵀ from TMEM (thread = head-dim index) into the accumulator.
+// TMEM columns: Sᵀ 0..127 (then Pᵀ in 0..31 and 64..95), dPᵀ (then dQ_iᵀ) 128..255,
 // dV 256..383, dK 384..511.
 #include "fa_kernels.h"
 #include "sm103.cuh"
@@ -49,17 +48,17 @@ constexpr int kD = 128;  // layout width: shared-memory tiles and TMEM columns a
 constexpr int kTile = 128;
 constexpr int kTileBytes = 128 * 128;   // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kOpBytes = 2 * kTileBytes;  // one 128 × 128 bf16 operand
-constexpr int kThreads = 512;  // four warpgroups: control, compute, two dQ drains
+constexpr int kThreads = 512;  // four warpgroups: control, two compute, dQ drain
 // Register split (setmaxnreg): the kernel launches with kRegsLaunch per thread
-// (all ptxas allows for 512 threads); the control and drain warpgroups give
-// registers to the compute warpgroup.  Each sub-partition holds one warp of
-// every warpgroup, so the split must fit 512 × kRegsLaunch; the launcher
-// refuses to run if ptxas assigned fewer registers than that.
+// (all ptxas allows for 512 threads); the control warpgroup gives registers to
+// the compute and drain warpgroups.  Each sub-partition holds one warp of every
+// warpgroup, so the split must fit 512 × kRegsLaunch; the launcher refuses to
+// run if ptxas assigned fewer registers than that.
 constexpr int kRegsLaunch = 128;
 constexpr int kRegsControl = 80;
-constexpr int kRegsCompute = 224;
-constexpr int kRegsDrain = 104;
-static_assert(128 * (kRegsControl + kRegsCompute + 2 * kRegsDrain) <= kThreads * kRegsLaunch, "register split");
+constexpr int kRegsCompute = 136;
+constexpr int kRegsDrain = 160;
+static_assert(128 * (kRegsControl + 2 * kRegsCompute + kRegsDrain) <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
@@ -207,9 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 2 * D);  // the drain warps that own head dims < D
-    mbar_init(&bars->p_ready, 128);
-    mbar_init(&bars->ds_ready, 128);
+    mbar_init(&bars->dq_free, D);  // the drain threads that own head dims < D
+    mbar_init(&bars->p_ready, 256);
+    mbar_init(&bars->ds_ready, 256);
     mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
@@ -315,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + kColDV, tmem + kColS + kk * 8, sdesc_sw128(dob + kk * 2048, kTileBytes, 1024), kIdescKM,
+          mma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                      sdesc_sw128(dob + kk * 2048, kTileBytes, 1024), kIdescKM,
                       (it > 0 || kk > 0) ? 1u : 0u);
         // Sᵀ_{i+1} overwrites Pᵀ_i, which the dV MMAs above read first (in order).
         if (it + 1 < nT) {
@@ -352,16 +352,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     reg_alloc<kRegsCompute>();
-    // -------------------------------------------- Pᵀ / dSᵀ, then dK / dV out
+    // ----------------------- Pᵀ / dSᵀ for 64 query columns, then dV or dK out
+    // Two warpgroups; warpgroup cw owns query columns 64·cw … 64·cw+63 of every
+    // tile (P and dS are elementwise per query column, so the halves never
+    // meet); thread = key row.  Each writes its Pᵀ over its own Sᵀ columns
+    // (64·cw …, 32 columns of bf16 pairs) and its dSᵀ into its own 64-column
+    // block of shared memory.
+    const int cw = (warp - 4) >> 2;
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;             // key row within the tile
+    const int r = wq * 32 + lane;               // key row within the tile
     const bool key_pad = j * kTile + r >= p.N;  // past N in a ragged last key tile
-    const int tr = threadIdx.x - 128;         // 0..127, for staging row stats
+    const int ct = threadIdx.x - 128 * (1 + cw);  // 0..127 within the warpgroup
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     uint8_t* sDST = smem + kOffDST;
+    float* lse_h = s_lse + cw * 64;  // this warpgroup's query columns
+    float* del_h = s_del + cw * 64;
+    const int bar_id = 1 + 2 * cw;   // named barriers 1 and 3 (2 ends the kernel)
     // The named barriers below are reached on every iteration by all four
     // warps; after an abort a warp keeps iterating without doing work, so no
     // warp is ever left waiting at a barrier another warp has abandoned.
@@ -370,56 +379,50 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const int i = i0 + it;
       const uint32_t ph = it & 1;
       const bool diag = p.causal && i == j;  // mask query columns c < r (key r > query c)
-      named_sync(1, 128);  // every thread is done reading the previous tile's stats
+      named_sync(bar_id, 128);  // every thread is done reading the previous tile's stats
       // Query rows past N (a ragged last tile) get LSE = +∞, so their P is 0.
-      const int qrow = i * kTile + tr;
-      s_lse[tr] = qrow < p.N ? p.lse_log2[bh * p.N + qrow] : INFINITY;
-      s_del[tr] = qrow < p.N ? p.delta[bh * p.N + qrow] : 0.f;
-      named_sync(1, 128);
+      if (ct < 64) {
+        const int qrow = i * kTile + cw * 64 + ct;
+        lse_h[ct] = qrow < p.N ? p.lse_log2[bh * p.N + qrow] : INFINITY;
+        del_h[ct] = qrow < p.N ? p.delta[bh * p.N + qrow] : 0.f;
+      }
+      named_sync(bar_id, 128);
       if (!ok) continue;
 
       ok = mbar_wait(&bars->s_full, ph, abort_flag, p.err, site(8));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; continue; }
       tc_fence_after();
-      // Pᵀ row = e^(σ Sᵀ row − LSE) as bf16 pairs, written back over Sᵀ (columns 0..63).
-      uint32_t pk[64];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      // Pᵀ row = e^(σ Sᵀ row − LSE) as bf16 pairs: pk[w] holds local query
+      // columns 2w, 2w + 1.
+      uint32_t pk[32];
+      {
         uint32_t ra[32], rb[32];
-        tmem_ld32(tmem + lane_base + kColS + half * 64, ra);
-        tmem_ld32(tmem + lane_base + kColS + half * 64 + 32, rb);
+        tmem_ld32(tmem + lane_base + kColS + cw * 64, ra);
+        tmem_ld32(tmem + lane_base + kColS + cw * 64 + 32, rb);
         tmem_wait_ld();
         reg_fence(ra);
         reg_fence(rb);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int c = half * 64 + 2 * e;
-          float a0 = ex2_approx(fmaf(__uint_as_float(ra[2 * e]), sl2, -s_lse[c]));
-          float a1 = ex2_approx(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -s_lse[c + 1]));
-          float b0 = ex2_approx(fmaf(__uint_as_float(rb[2 * e]), sl2, -s_lse[c + 32]));
-          float b1 = ex2_approx(fmaf(__uint_as_float(rb[2 * e + 1]), sl2, -s_lse[c + 33]));
+          const int c = 2 * e;
+          float a0 = ex2_approx(fmaf(__uint_as_float(ra[2 * e]), sl2, -lse_h[c]));
+          float a1 = ex2_approx(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -lse_h[c + 1]));
+          float b0 = ex2_approx(fmaf(__uint_as_float(rb[2 * e]), sl2, -lse_h[c + 32]));
+          float b1 = ex2_approx(fmaf(__uint_as_float(rb[2 * e + 1]), sl2, -lse_h[c + 33]));
           if (diag) {
-            a0 = c < r ? 0.f : a0;
-            a1 = c + 1 < r ? 0.f : a1;
-            b0 = c + 32 < r ? 0.f : b0;
-            b1 = c + 33 < r ? 0.f : b1;
+            const int cg = cw * 64 + c;  // query column within the tile
+            a0 = cg < r ? 0.f : a0;
+            a1 = cg + 1 < r ? 0.f : a1;
+            b0 = cg + 32 < r ? 0.f : b0;
+            b1 = cg + 33 < r ? 0.f : b1;
           }
           if (key_pad) a0 = a1 = b0 = b1 = 0.f;  // zero-filled K row: score 0, not −∞
-          pk[half * 32 + e] = pack_bf16x2(a0, a1);
-          pk[half * 32 + 16 + e] = pack_bf16x2(b0, b1);
+          pk[e] = pack_bf16x2(a0, a1);
+          pk[16 + e] = pack_bf16x2(b0, b1);
         }
       }
-      {
-        uint32_t w0[32], w1[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          w0[e] = pk[e];
-          w1[e] = pk[32 + e];
-        }
-        tmem_st32(tmem + lane_base + kColS, w0);
-        tmem_st32(tmem + lane_base + kColS + 32, w1);
-        tmem_wait_st();
-      }
+      tmem_st32(tmem + lane_base + kColS + cw * 64, pk);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
 
@@ -428,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       if (!__all_sync(0xffffffffu, ok)) { ok = false; continue; }
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t rd[32];
-        tmem_ld32(tmem + lane_base + kColDP + cc * 32, rd);
+        tmem_ld32(tmem + lane_base + kColDP + cw * 64 + cc * 32, rd);
         tmem_wait_ld();
         reg_fence(rd);
 #pragma unroll
@@ -438,13 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           uint32_t w[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
-            const int c = cc * 32 + q4 * 8 + 2 * e2;           // query column
+            const int c = cc * 32 + q4 * 8 + 2 * e2;  // local query column
             const uint32_t pw = pk[c >> 1];
-            const float d0 = bf16lo(pw) * (__uint_as_float(rd[q4 * 8 + 2 * e2]) - s_del[c]);
-            const float d1 = bf16hi(pw) * (__uint_as_float(rd[q4 * 8 + 2 * e2 + 1]) - s_del[c + 1]);
+            const float d0 = bf16lo(pw) * (__uint_as_float(rd[q4 * 8 + 2 * e2]) - del_h[c]);
+            const float d1 = bf16hi(pw) * (__uint_as_float(rd[q4 * 8 + 2 * e2 + 1]) - del_h[c + 1]);
             w[e2] = pack_bf16x2(d0, d1);
           }
-          const int c8 = cc * 4 + q4;
+          const int c8 = cw * 8 + cc * 4 + q4;  // 16-byte chunk (8 query columns) within the row
           *reinterpret_cast<uint4*>(sDST + (c8 >> 3) * kTileBytes + r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
@@ -457,39 +460,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       ok = mbar_wait(&bars->acc_done, 0, abort_flag, p.err, site(11));
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
+        // Warpgroup 0 writes dV, warpgroup 1 dK (with σ).
         const int64_t grow = bh * p.N + static_cast<int64_t>(j) * kTile + r;
-        __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + grow * D;
-        __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + grow * D;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(cw == 0 ? p.dv : p.dk) + grow * D;
+        const uint32_t col = cw == 0 ? kColDV : kColDK;
+        const float mul = cw == 0 ? 1.f : p.scale;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + kColDV + cc * 32, rr);
+          tmem_ld32(tmem + lane_base + col + cc * 32, rr);
           tmem_wait_ld();
           reg_fence(rr);
-          if (!key_pad) store_row32(dv_row + cc * 32, rr, 1.f);
-        }
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + kColDK + cc * 32, rr);
-          tmem_wait_ld();
-          reg_fence(rr);
-          if (!key_pad) store_row32(dk_row + cc * 32, rr, p.scale);
+          if (!key_pad) store_row32(out + cc * 32, rr, mul);
         }
       }
     }
     tc_fence_before();
     named_sync(2, kThreads);
   } else {
-    reg_dealloc<kRegsDrain>();
+    reg_alloc<kRegsDrain>();
     // ------------------------------------------------------ dQ_iᵀ drain
-    // Two warpgroups, each owning 64 of dQ_iᵀ's 128 query columns.  A 4 × 4
-    // exchange among neighbouring lanes turns "lane = head-dim index" into four
-    // consecutive head dims of one query row per lane, so every reduction
+    // Thread = head-dim index (TMEM lane).  Each warp loads all 128 query
+    // columns of dQ_iᵀ, frees the columns for the next dPᵀ, then adds them: a
+    // 4 × 4 exchange among neighbouring lanes turns "lane = head-dim index" into
+    // four consecutive head dims of one query row per lane, so every reduction
     // instruction adds 16 bytes per lane: four full 128-byte lines per warp.
-    // TMEM lane = head dim, so with D < 128 the warps of lane quarters at or
-    // past D have nothing to drain (they hold the zero rows) and sit this out.
-    const int half = (warp - 8) >> 2;
+    // With D < 128 the warps of lane quarters at or past D have nothing to
+    // drain (they hold the zero rows) and sit this out.
     const int wq = warp & 3;
     const int r4 = lane & 3;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
@@ -498,19 +495,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const bool ok = mbar_wait_inl(&bars->dq_full, it & 1, abort_flag, p.err, site(12));
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tmem + lane_base + kColDP + half * 64, r0);
-      tmem_ld32(tmem + lane_base + kColDP + half * 64 + 32, r1);
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(tmem + lane_base + kColDP, r0);
+      tmem_ld32(tmem + lane_base + kColDP + 32, r1);
+      tmem_ld32(tmem + lane_base + kColDP + 64, r2);
+      tmem_ld32(tmem + lane_base + kColDP + 96, r3);
       tmem_wait_ld();
       reg_fence(r0);
       reg_fence(r1);
+      reg_fence(r2);
+      reg_fence(r3);
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
       // Column c of dQ_iᵀ is query row i·128 + c; lane 4g + r4 ends up with query
       // row c0 + r4, head dims wq·32 + 4g … +3.
       float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * D + wq * 32 + (lane & ~3);
-      reduce_cols<D>(r0, dst, half * 64, r4, p.N - i * kTile);
-      reduce_cols<D>(r1, dst, half * 64 + 32, r4, p.N - i * kTile);
+      const int rows_valid = p.N - i * kTile;
+      reduce_cols<D>(r0, dst, 0, r4, rows_valid);
+      reduce_cols<D>(r1, dst, 32, r4, rows_valid);
+      reduce_cols<D>(r2, dst, 64, r4, rows_valid);
+      reduce_cols<D>(r3, dst, 96, r4, rows_valid);
     }
     tc_fence_before();
     named_sync(2, kThreads);
