@@ -25,17 +25,20 @@
 // 4 × 4 exchange among neighbouring lanes then gives each lane four consecutive
 // head dims of one query row, and every 16-byte-per-lane reduction covers four
 // full 128-byte lines.  Those reductions (as many bytes as the whole fp32 dQ
-// once per key tile) are what the L2 has to absorb.
+// once per key tile) are what the L2 has to absorb, and it absorbs them faster
+// the more warps issue them, so two warpgroups do, each for half of the query
+// columns.
 //
 // Causal mask (query i sees key j when j <= i): key tile j only meets query
 // tiles i >= j, so the loop starts at its diagonal tile, where Pᵀ entries with
 // key > query are zeroed (and with them dSᵀ).
 //
-// Warp roles (512 threads, four warpgroups, registers rebalanced with
+// Warp roles (640 threads, five warpgroups, registers rebalanced with
 // setmaxnreg): warp 0 TMA producer and warp 1 TMEM owner + MMA issuer (warps 2,
 // 3 idle); warps 4..7 and 8..11 compute Pᵀ and dSᵀ (thread = key row) for query
-// columns 0..63 and 64..127 and write dV and dK at the end; warps 12..15 drain
-// dQ_iᵀ from TMEM (thread = head-dim index) into the accumulator.
+// columns 0..63 and 64..127 and write dV and dK at the end; warps 12..15 and
+// 16..19 drain dQ_iᵀ columns 0..63 and 64..127 from TMEM (thread = head-dim
+// index) into the accumulator.
 // TMEM columns: Sᵀ 0..127 (then Pᵀ in 0..31 and 64..95), dPᵀ (then dQ_iᵀ) 128..255,
 // dV 256..383, dK 384..511.
 #include "fa_kernels.h"
@@ -48,17 +51,18 @@ constexpr int kD = 128;  // layout width: shared-memory tiles and TMEM columns a
 constexpr int kTile = 128;
 constexpr int kTileBytes = 128 * 128;   // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kOpBytes = 2 * kTileBytes;  // one 128 × 128 bf16 operand
-constexpr int kThreads = 512;  // four warpgroups: control, two compute, dQ drain
+constexpr int kThreads = 640;  // five warpgroups: control, two compute, two dQ drains
 // Register split (setmaxnreg): the kernel launches with kRegsLaunch per thread
-// (all ptxas allows for 512 threads); the control warpgroup gives registers to
-// the compute and drain warpgroups.  Each sub-partition holds one warp of every
-// warpgroup, so the split must fit 512 × kRegsLaunch; the launcher refuses to
-// run if ptxas assigned fewer registers than that.
-constexpr int kRegsLaunch = 128;
-constexpr int kRegsControl = 80;
-constexpr int kRegsCompute = 136;
-constexpr int kRegsDrain = 160;
-static_assert(128 * (kRegsControl + 2 * kRegsCompute + kRegsDrain) <= kThreads * kRegsLaunch, "register split");
+// (all ptxas allows for 640 threads, five warps per sub-partition); the control
+// and drain warpgroups give registers to the compute warpgroups.  Each
+// sub-partition holds one warp of every warpgroup, so the split must fit
+// 640 × kRegsLaunch; the launcher refuses to run if ptxas assigned fewer
+// registers than that.
+constexpr int kRegsLaunch = 96;
+constexpr int kRegsControl = 56;
+constexpr int kRegsCompute = 120;
+constexpr int kRegsDrain = 88;
+static_assert(128 * (kRegsControl + 2 * kRegsCompute + 2 * kRegsDrain) <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, D);  // the drain threads that own head dims < D
+    mbar_init(&bars->dq_free, 2 * D);  // the drain threads that own head dims < D
     mbar_init(&bars->p_ready, 256);
     mbar_init(&bars->ds_ready, 256);
     mbar_init(&bars->ds_free, 1);
@@ -478,15 +482,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     tc_fence_before();
     named_sync(2, kThreads);
   } else {
-    reg_alloc<kRegsDrain>();
+    reg_dealloc<kRegsDrain>();
     // ------------------------------------------------------ dQ_iᵀ drain
-    // Thread = head-dim index (TMEM lane).  Each warp loads all 128 query
-    // columns of dQ_iᵀ, frees the columns for the next dPᵀ, then adds them: a
-    // 4 × 4 exchange among neighbouring lanes turns "lane = head-dim index" into
+    // Thread = head-dim index (TMEM lane); warpgroup `half` owns query columns
+    // 64·half … 64·half+63.  Each warp loads its 64 columns of dQ_iᵀ, frees them
+    // for the next dPᵀ (once both warpgroups have), then adds them: a 4 × 4
+    // exchange among neighbouring lanes turns "lane = head-dim index" into
     // four consecutive head dims of one query row per lane, so every reduction
     // instruction adds 16 bytes per lane: four full 128-byte lines per warp.
     // With D < 128 the warps of lane quarters at or past D have nothing to
     // drain (they hold the zero rows) and sit this out.
+    const int half = (warp - 12) >> 2;
     const int wq = warp & 3;
     const int r4 = lane & 3;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
@@ -495,26 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const bool ok = mbar_wait_inl(&bars->dq_full, it & 1, abort_flag, p.err, site(12));
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tmem + lane_base + kColDP, r0);
-      tmem_ld32(tmem + lane_base + kColDP + 32, r1);
-      tmem_ld32(tmem + lane_base + kColDP + 64, r2);
-      tmem_ld32(tmem + lane_base + kColDP + 96, r3);
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem + lane_base + kColDP + half * 64, r0);
+      tmem_ld32(tmem + lane_base + kColDP + half * 64 + 32, r1);
       tmem_wait_ld();
       reg_fence(r0);
       reg_fence(r1);
-      reg_fence(r2);
-      reg_fence(r3);
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
       // Column c of dQ_iᵀ is query row i·128 + c; lane 4g + r4 ends up with query
       // row c0 + r4, head dims wq·32 + 4g … +3.
       float* dst = p.dq_acc + (bh * p.N + static_cast<int64_t>(i) * kTile) * D + wq * 32 + (lane & ~3);
       const int rows_valid = p.N - i * kTile;
-      reduce_cols<D>(r0, dst, 0, r4, rows_valid);
-      reduce_cols<D>(r1, dst, 32, r4, rows_valid);
-      reduce_cols<D>(r2, dst, 64, r4, rows_valid);
-      reduce_cols<D>(r3, dst, 96, r4, rows_valid);
+      reduce_cols<D>(r0, dst, half * 64, r4, rows_valid);
+      reduce_cols<D>(r1, dst, half * 64 + 32, r4, rows_valid);
     }
     tc_fence_before();
     named_sync(2, kThreads);
