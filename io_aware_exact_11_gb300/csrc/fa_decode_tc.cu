@@ -29,14 +29,9 @@
 // requested at an out-of-range row so TMA fills them with zeros, and on a
 // split's last, partial tile the softmax warp zeroes the V rows past the end
 // (slots of a partly filled page hold stale data) before P̃V runs.
-// Pages of fewer than 64 keys make TMA boxes so small (2 KB at 16 keys) that
-// the copy engine's per-box cost caps the stream far below HBM bandwidth; so
-// do per-thread 16-byte copies, which run out of outstanding requests.  For
-// them (LOADER) the producer bulk-copies each page (contiguous in the cache)
-// into the ring slot in plain row order, and four more warps rewrite the slot
-// in place into the swizzled layout (all read into registers, a barrier, all
-// write), zeroing keys past the end, fence the writes for the tensor cores'
-// async-proxy reads and arrive on the tile's barrier.
+// The boxes of one tile are issued by different lanes of the producer warp at
+// once; small pages (2 KB boxes at 16 keys) need that to keep enough copies in
+// flight.
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -48,7 +43,6 @@ constexpr int kTileBytes = 128 * 128;    // [128 rows][64 bf16], 128-byte swizzl
 constexpr int kSlot = 2 * kTileBytes;    // one 128 × 128 bf16 tile
 constexpr int kRing = 5;
 constexpr int kThreads = 96;
-constexpr int kLoaderThreads = 128;  // the LOADER variant's copy warps (warps 3..6)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
@@ -63,7 +57,6 @@ constexpr int kSmem = kOffBar + 256 + 1024;
 struct Bars {
   uint64_t q_full;
   uint64_t r_full[kRing], r_empty[kRing];
-  uint64_t r_stage[kRing];  // LOADER: the slot's pages have landed in row order
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, p_free;
   uint64_t drain;
@@ -76,13 +69,8 @@ __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernDeco
 __device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int seq_v(int j, int T) { return min(2 * j + 2, 2 * T - 1); }
 
-__device__ __forceinline__ void loader_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kLoaderThreads) : "memory");
-}
-
-template <bool PAGED, bool LOADER>
-__global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads, 1)
-    decode_gqa_tc_kernel(const __grid_constant__ DecodeTcParams p) {
+template <bool PAGED>
+__global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid_constant__ DecodeTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -113,9 +101,8 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kRing; ++s) {
-      mbar_init(&bars->r_full[s], LOADER ? kLoaderThreads : 1);
+      mbar_init(&bars->r_full[s], 1);
       mbar_init(&bars->r_empty[s], 1);
-      mbar_init(&bars->r_stage[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
@@ -164,44 +151,7 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
       }
       return blk;
     };
-    if (LOADER && T > 0) {
-      // Whole pages in row order, one bulk copy per lane so the copies of a
-      // tile's pages are issued together; pages past the sequence (a suffix of
-      // the tile) are not fetched: the copy warps write zeros there.
-      if (lane == 0) {
-        tma_prefetch_desc(&p.tm_q);
-        mbar_arrive_expect_tx(&bars->q_full, kSlot);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_4d(smem + kOffQ + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64, qrow0, 0, 0);
-      }
-      const int bs = p.block_size;
-      const uint32_t page_bytes = static_cast<uint32_t>(bs) * 256;
-      int issued = 0;
-      for (int t = 0; t < 2 * T; ++t) {
-        const int slot = t % kRing;
-        const bool is_v = t != 0 && (t == 2 * T - 1 || !(t & 1));
-        const int jt = t == 0 ? 0 : (t == 2 * T - 1 ? T - 1 : ((t & 1) ? (t + 1) >> 1 : (t - 2) >> 1));
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&bars->r_empty[slot], ((t / kRing) & 1) ^ 1, abort_flag, p.err, site(1));
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        int npg = 0;
-        while (npg < kBN / bs && key0 + jt * kBN + npg * bs < kend) ++npg;
-        if (lane == 0) mbar_arrive_expect_tx(&bars->r_stage[slot], npg * page_bytes);
-        __syncwarp();
-        if (lane < npg) {
-          const uint8_t* base = static_cast<const uint8_t*>(is_v ? p.v_pages : p.k_pages);
-          const int blk = page_id(key0 + jt * kBN + lane * bs);
-          bulk_load(smem + kOffR + slot * kSlot + lane * page_bytes,
-                    base + (static_cast<int64_t>(blk) * p.Hkv + hkv) * page_bytes, page_bytes, &bars->r_stage[slot]);
-        }
-        ++issued;
-      }
-      if (lane == 0 && *abort_flag) {
-        mbar_wait_drain(&bars->q_full, 0, 200000000ull);
-        for (int t = (issued > kRing ? issued - kRing : 0); t < issued; ++t)
-          mbar_wait_drain(&bars->r_stage[t % kRing], (t / kRing) & 1, 200000000ull);
-      }
-    } else if (!LOADER && T > 0) {
+    if (T > 0) {
       // TMA boxes, issued warp-wide: lane 0 waits for the slot and arms its
       // byte count, then lane kb (contiguous cache) or lane pg (one page,
       // both 64-column halves) issues its boxes.
@@ -300,40 +250,6 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
         mbar_wait_drain(&bars->drain, 0, 200000000ull);
       }
     }
-  } else if (LOADER && warp >= 3) {
-    // ------------------------------------- row order → swizzled layout (LOADER)
-    // Thread lt owns 16-byte chunk c16 = lt % 16 of rows lt/16, lt/16 + 8, …;
-    // in row order those are consecutive (conflict-free reads), and sixteen
-    // threads write one row's 256 bytes as two 128-byte swizzled rows.
-    const int lt = threadIdx.x - kThreads;  // 0..127
-    const int c16 = lt & 15;
-    const int rbase = lt >> 4;
-    // Every loader thread reaches the barrier on every tile, even after an
-    // abort, so none is left waiting for a thread that stopped.
-    bool ok = true;
-    for (int t = 0; t < 2 * T; ++t) {
-      const int slot = t % kRing;
-      const int jt = t == 0 ? 0 : (t == 2 * T - 1 ? T - 1 : ((t & 1) ? (t + 1) >> 1 : (t - 2) >> 1));
-      uint8_t* sl = smem + kOffR + slot * kSlot;
-      uint4 v[16];
-      if (ok) ok = mbar_wait(&bars->r_stage[slot], (t / kRing) & 1, abort_flag, p.err, site(11));
-      if (ok) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = *reinterpret_cast<const uint4*>(sl + (rbase + 8 * i) * 256 + c16 * 16);
-      }
-      loader_sync();
-      if (ok) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int row = rbase + 8 * i;
-          const bool live = key0 + jt * kBN + row < kend;
-          *reinterpret_cast<uint4*>(sl + (c16 >> 3) * kTileBytes + row * 128 + (((c16 & 7) ^ (row & 7)) << 4)) =
-              live ? v[i] : make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->r_full[slot]);
-      }
-    }
   } else {
     // ------------------------------------------- softmax for rows 0..31, epilogue
     const int row = lane;  // TMEM lane; rows < G are the group's query heads
@@ -428,7 +344,7 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
         }
       }
       tmem_wait_st();
-      if (PAGED && !LOADER && valid < kBN) {
+      if (PAGED && valid < kBN) {
         // Zero the V rows past the sequence end once V_j has landed.
         const int t = seq_v(j, T);
         ok = mbar_wait(&bars->r_full[t % kRing], (t / kRing) & 1, abort_flag, p.err, site(10));
@@ -489,27 +405,23 @@ __global__ void __launch_bounds__(LOADER ? kThreads + kLoaderThreads : kThreads,
   }
 }
 
-template <bool PAGED, bool LOADER>
+template <bool PAGED>
 cudaError_t launch_gqa(const DecodeTcParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_gqa_tc_kernel<PAGED, LOADER>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_gqa_tc_kernel<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  decode_gqa_tc_kernel<PAGED, LOADER>
-      <<<dim3(p.n_splits, p.Hkv, p.B), LOADER ? kThreads + kLoaderThreads : kThreads, kSmem, stream>>>(p);
+  decode_gqa_tc_kernel<PAGED><<<dim3(p.n_splits, p.Hkv, p.B), kThreads, kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode_gqa_tc(const DecodeTcParams& p, cudaStream_t stream) {
-  return launch_gqa<false, false>(p, stream);
+  return launch_gqa<false>(p, stream);
 }
 
 cudaError_t launch_decode_gqa_tc_paged(const DecodeTcParams& p, cudaStream_t stream) {
   if (p.block_size < 16 || p.block_size > kBN || (kBN % p.block_size) != 0) return cudaErrorInvalidValue;
-  // Pages under 64 keys: per-thread copies; larger pages: one TMA box per page piece.
-  if (p.block_size < 64) return launch_gqa<true, true>(p, stream);
-  return launch_gqa<true, false>(p, stream);
+  return launch_gqa<true>(p, stream);
 }
 
 }  // namespace fa
