@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
-    "fwd_prefill": {"src": "ae5ff0df3d5a5b5f", "bytes": 402714368 + 119067136},
+    "fwd_prefill": {"src": "d6ca9862a3d45992", "bytes": 402712064 + 117227008},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
     "bwd_train": {"src": "91820ae77d5cc5b2", "bytes": 404957696 + 218157056},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is

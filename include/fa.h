@@ -91,7 +91,8 @@ FA_API fa_status fa_forward(const void* q, const void* k, const void* v, void* o
  * fa_forward_masked — fa_forward with a mask (FA_MASK_NONE is fa_forward).
  *   With FA_MASK_CAUSAL masked scores are −∞ before the softmax; a CTA streams
  *   only the key tiles its rows can see.  N_q > N_kv with a causal mask gives
- *   FA_ERR_INVALID_ARG.  Same arguments, layouts and support as fa_forward.
+ *   FA_ERR_INVALID_ARG; a causal N_q above 65535·256 gives FA_ERR_UNSUPPORTED.
+ *   Same arguments, layouts and support as fa_forward.
  */
 FA_API fa_status fa_forward_masked(const void* q, const void* k, const void* v, void* o, float* lse,
                                    int B, int H, int N_q, int N_kv, int d, fa_dtype dtype, float scale,

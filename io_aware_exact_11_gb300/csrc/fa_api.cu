@@ -160,6 +160,8 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     return fail(FA_ERR_INVALID_ARG, "fa_forward: lse must be 4-byte aligned");
   if (causal && N_q > N_kv)
     return fail(FA_ERR_INVALID_ARG, "fa_forward: causal attention needs N_q <= N_kv (got %d > %d)", N_q, N_kv);
+  if (causal && (N_q + 255) / 256 > 65535)  // the causal grid puts the 256-row query blocks on its z axis
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward: causal attention needs N_q <= %d", 65535 * 256);
   const int esz = dtype == FA_BF16 ? 2 : 4;
   int64_t st[12];
   if (strides == nullptr) {
@@ -258,6 +260,8 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, f
     return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: lse must be 4-byte aligned");
   if (mask == FA_MASK_CAUSAL && N_q > N_kv)
     return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: causal attention needs N_q <= N_kv");
+  if (mask == FA_MASK_CAUSAL && (N_q + 255) / 256 > 65535)
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp8: causal attention needs N_q <= %d", 65535 * 256);
   fa::FwdParams p;
   memset(&p, 0, sizeof(p));
   const int64_t nq = static_cast<int64_t>(N_q) * d, nk = static_cast<int64_t>(N_kv) * d;

@@ -41,7 +41,9 @@
 // Causal mask (the lesson's §5 lab uses is_causal=True), bottom-right aligned:
 // row i sees keys j <= i + (N_kv − N_q).  A CTA streams only the key tiles its
 // last row can see; rows mask the rest of their diagonal tile with −∞, and
-// the heaviest query blocks are scheduled first.
+// the heaviest query blocks of every head are scheduled first (the causal grid
+// is (H, B, query blocks), so all heads' longest blocks go out in the first
+// waves and the shortest ones fill the tail).
 //
 // FP8 (E4M3) variant, FlashAttention-3's addition noted in the lesson (§3.3) and
 // the interview notes (§四.5): Q, K, V arrive as E4M3 with per-tensor descale
@@ -140,10 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int mt = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  // Causal grids are (H, B, query blocks), heaviest blocks of every head first.
+  const int mt = p.causal ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x);
   const int m0 = mt * (kQT * kBM);
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
+  const int h = p.causal ? blockIdx.x : blockIdx.y;
+  const int b = p.causal ? blockIdx.y : blockIdx.z;
   const int off = p.Nkv - p.Nq;  // >= 0 whenever causal
   const int kv_end = p.causal ? min(p.Nkv, m0 + kQT * kBM + off) : p.Nkv;
   const int T = (kv_end + kBN - 1) / kBN;
@@ -428,7 +431,8 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(fwd_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.Nq + kQT * kBM - 1) / (kQT * kBM), p.H, p.B);
+  const unsigned n_mt = (p.Nq + kQT * kBM - 1) / (kQT * kBM);
+  const dim3 grid = p.causal ? dim3(p.H, p.B, n_mt) : dim3(n_mt, p.H, p.B);
   fwd_kernel<D, FP8><<<grid, kThreads, L::kSmem, stream>>>(p);
   return cudaGetLastError();
 }

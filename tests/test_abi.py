@@ -128,6 +128,9 @@ def test_masked_entry_points_validate_before_cuda(L):
     assert fwdm(mask=5) == fa.FA_ERR_INVALID_ARG
     assert fwdm(nq=200, nkv=100) == fa.FA_ERR_INVALID_ARG      # causal needs N_q <= N_kv
     assert b"causal" in L.fa_get_last_error()
+    # The causal grid holds at most 65535 blocks of 256 query rows.
+    big = 65535 * 256 + 1
+    assert fwdm(nq=big, nkv=big) == fa.FA_ERR_UNSUPPORTED
 
     def bwdm(mask=fa.FA_MASK_CAUSAL, n=200):
         return L.fa_backward_masked(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, n, 128, fa.FA_BF16,
