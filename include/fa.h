@@ -281,7 +281,8 @@ FA_API fa_status fa_backward(const void* q, const void* k, const void* v, const 
  * fa_backward_masked — fa_backward for a forward run with `mask` (FA_MASK_NONE
  *   is fa_backward).  With FA_MASK_CAUSAL (query i sees key j <= i) each key
  *   tile only visits the query tiles at or after its diagonal.  Same arguments,
- *   workspace and support as fa_backward.
+ *   workspace and support as fa_backward; a causal N above 65535·128 gives
+ *   FA_ERR_UNSUPPORTED.
  */
 FA_API fa_status fa_backward_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                     const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,

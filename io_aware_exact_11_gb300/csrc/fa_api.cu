@@ -768,6 +768,8 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   if (dtype != FA_BF16 || (d != 64 && d != 128))
     return fail(FA_ERR_UNSUPPORTED, "fa_backward: only bf16 with d = 64 or 128 is built");
   if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_backward: B and H must be <= 65535");
+  if (causal && (N + 127) / 128 > 65535)  // the causal grid puts the 128-key tiles on its z axis
+    return fail(FA_ERR_UNSUPPORTED, "fa_backward: causal backward needs N <= %d", 65535 * 128);
   if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_backward: scale must be finite and > 0");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))

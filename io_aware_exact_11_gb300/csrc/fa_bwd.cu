@@ -193,9 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int j = blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
+  // Causal grids are (H, B, key tiles): key tile j meets T − j query tiles, so
+  // every head's longest tiles (small j) launch first.
+  const int j = p.causal ? blockIdx.z : blockIdx.x;
+  const int h = p.causal ? blockIdx.x : blockIdx.y;
+  const int b = p.causal ? blockIdx.y : blockIdx.z;
   const int64_t bh = static_cast<int64_t>(b) * p.H + h;
   const int T = (p.N + kTile - 1) / kTile;  // the last tile may be ragged
   const int i0 = p.causal ? j : 0;  // first query tile this key tile meets
@@ -542,7 +544,9 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, int* launches)
   cudaFuncAttributes attr;
   if ((e = cudaFuncGetAttributes(&attr, bwd_main_kernel<D>)) != cudaSuccess) return e;
   if (attr.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
-  bwd_main_kernel<D><<<dim3((p.N + kTile - 1) / kTile, p.H, p.B), kThreads, kSmem, stream>>>(p);
+  const unsigned n_kt = (p.N + kTile - 1) / kTile;
+  const dim3 grid = p.causal ? dim3(p.H, p.B, n_kt) : dim3(n_kt, p.H, p.B);
+  bwd_main_kernel<D><<<grid, kThreads, kSmem, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n4 = rows * D / 4;

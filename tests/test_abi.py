@@ -137,6 +137,7 @@ def test_masked_entry_points_validate_before_cuda(L):
                                     0.1, FAKE, 1 << 24, mask, None)
     assert bwdm(mask=-1) == fa.FA_ERR_INVALID_ARG
     assert bwdm(n=0) == fa.FA_ERR_INVALID_ARG
+    assert bwdm(n=65535 * 128 + 1) == fa.FA_ERR_UNSUPPORTED   # the causal grid holds 65535 key tiles
 
 
 def test_gqa_decode_validates_before_cuda(L):
