@@ -296,6 +296,17 @@ FA_API fa_status fa_backward_masked(const void* q, const void* k, const void* v,
  */
 FA_API fa_status fa_device_status(void* stream);
 
+/*
+ * fa_watchdog_selftest — exercises the failure path of the bounded pipeline
+ *   waits on the device: enqueues one CTA whose thread waits on a barrier that
+ *   nothing completes.  After the wait limit (1 s) the wait gives up and
+ *   records its site, exactly as a stuck pipeline would, and the kernel
+ *   returns; the next fa_device_status(stream) reports FA_ERR_DEVICE_TIMEOUT
+ *   ("kernel 15 gave up waiting at site 1") and clears the flag.  Nothing
+ *   faults and the context stays usable.  Returns FA_OK once enqueued.
+ */
+FA_API fa_status fa_watchdog_selftest(void* stream);
+
 /* Static description of a status code. */
 FA_API const char* fa_status_string(fa_status s);
 

@@ -13,6 +13,24 @@
 
 #include "../../include/fa.h"
 #include "fa_kernels.h"
+#include "sm103.cuh"
+
+namespace fa {
+// One thread waits, with the same bounded wait every pipeline kernel uses, on
+// an mbarrier that nothing completes.  The wait gives up after its limit,
+// records (kKernSelftest << 8) | 1 in the watchdog word and the kernel returns:
+// the failure path of a stuck pipeline, with nothing faulting or hanging.
+__global__ void watchdog_selftest_kernel(unsigned int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_wait(&bar, 0, &abort_flag, err, (kKernSelftest << 8) | 1u);
+  }
+}
+}  // namespace fa
 
 namespace {
 
@@ -829,6 +847,14 @@ fa_status fa_backward_masked(const void* q, const void* k, const void* v, const 
     return fail(FA_ERR_INVALID_ARG, "fa_backward_masked: unknown mask %d", static_cast<int>(mask));
   return backward_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, dtype, scale, workspace, workspace_bytes,
                        mask == FA_MASK_CAUSAL ? 1 : 0, stream);
+}
+
+fa_status fa_watchdog_selftest(void* stream) {
+  unsigned int* word = nullptr;
+  fa_status r = watchdog_ptr(&word);
+  if (r != FA_OK) return r;
+  fa::watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(word);
+  return check_launch("fa_watchdog_selftest", 1);
 }
 
 fa_status fa_device_status(void* stream) {

@@ -13,6 +13,7 @@ enum : unsigned int {
   kKernFwd = 1,
   kKernDecode = 2,
   kKernBwd = 3,
+  kKernSelftest = 15,  // fa_watchdog_selftest
 };
 
 struct FwdParams {

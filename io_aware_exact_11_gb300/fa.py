@@ -37,6 +37,7 @@ EXPORTED = (
     "fa_backward",
     "fa_backward_masked",
     "fa_device_status",
+    "fa_watchdog_selftest",
     "fa_status_string",
     "fa_get_last_error",
     "fa_launch_count",
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.fa_backward_masked.restype = i32
         L.fa_device_status.argtypes = [vp]
         L.fa_device_status.restype = i32
+        L.fa_watchdog_selftest.argtypes = [vp]
+        L.fa_watchdog_selftest.restype = i32
         L.fa_status_string.argtypes = [i32]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_get_last_error.restype = ctypes.c_char_p
@@ -142,6 +145,12 @@ def launch_count() -> int:
 def device_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel's bounded wait gave up."""
     _check(lib().fa_device_status(_stream_ptr(stream)))
+
+
+def watchdog_selftest(stream=None) -> None:
+    """Enqueue a kernel whose bounded wait runs out (~1 s); the next
+    device_status() raises FAError with FA_ERR_DEVICE_TIMEOUT."""
+    _check(lib().fa_watchdog_selftest(_stream_ptr(stream)))
 
 
 def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True, stream=None,
