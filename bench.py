@@ -46,7 +46,7 @@ NCU_TRAFFIC = {
     # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
     "fwd_prefill": {"src": "d6ca9862a3d45992", "bytes": 402712064 + 117227008},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
-    "bwd_train": {"src": "91820ae77d5cc5b2", "bytes": 404957696 + 218157056},
+    "bwd_train": {"src": "b4f7746084f19789", "bytes": 405110016 + 219461376},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
     # proportional to B, stored here scaled to the B=64 launch
     "decode_split": {"src": "8261e7e17c87db05", "bytes": (1073901568 + 6750464) * 8},
