@@ -605,8 +605,8 @@ fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, voi
   if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: unknown dtype");
   if (dtype != FA_BF16 || d != 128)
     return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: only bf16 with d=128 is built");
-  if (H_q / H_kv > 32)
-    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: at most 32 query heads per key/value head (got %d)",
+  if (H_q / H_kv > 128)  // the group's rows share one 128-row MMA tile
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: at most 128 query heads per key/value head (got %d)",
                 H_q / H_kv);
   if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: n_splits must be <= 256");
   if (B > 65535 || H_q > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: B and H must be <= 65535");
@@ -684,8 +684,8 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
   if (dtype != FA_BF16 || d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: only bf16 with d=128 is built");
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
     return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: block_size must be 16, 32, 64 or 128 (got %d)", block_size);
-  if (H_q / H_kv > 32)
-    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: at most 32 query heads per key/value head");
+  if (H_q / H_kv > 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: at most 128 query heads per key/value head");
   if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: n_splits must be <= 256");
   if (B > 65535 || H_q > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: B and H must be <= 65535");
   if (static_cast<int64_t>(max_blocks) * block_size > (1 << 30))

@@ -12,10 +12,12 @@
 // split-KV merge kernel folds with the block-merge rule (omica.com.cn news
 // 1422242, §二.3).
 //
-// Warp roles (96 threads): warp 0 softmax for TMEM lanes 0..31 (rows 0..31 of
-// the A tile; rows ≥ G are padding) and the epilogue; warp 1 TMA producer
-// (Q once, then K_0, K_1, V_0, K_2, V_1, … into a 5-slot ring); warp 2 TMEM
-// owner and MMA issuer.  TMEM: S buffers at columns 0 and 128, O at 256.
+// Warp roles (224 threads): warps 0..3 softmax and epilogue for TMEM lanes
+// 32·w … 32·w+31 (rows of the A tile; rows ≥ G are padding, and only the
+// ⌈G/32⌉ warps that hold query rows take part); warp 5 TMA producer (Q once,
+// then K_0, K_1, V_0, K_2, V_1, … into a 5-slot ring); warp 6 TMEM owner and
+// MMA issuer; warp 4 idle.  Warp w runs on SM sub-partition w % 4, so with
+// G ≤ 32 softmax, producer and MMA issuer each have a sub-partition of their own.  TMEM: S buffers at columns 0 and 128, O at 256.
 // P̃ is written as bf16 pairs over its S buffer and read from TMEM by the P̃V
 // MMA; S(j) is issued after P̃V(j−2), so the in-order tensor pipe has read
 // P̃(j−2) before S(j) overwrites it.  Keeping P̃ out of shared memory leaves
@@ -42,7 +44,7 @@ constexpr int kBN = 128;
 constexpr int kTileBytes = 128 * 128;    // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kSlot = 2 * kTileBytes;    // one 128 × 128 bf16 tile
 constexpr int kRing = 5;
-constexpr int kThreads = 96;
+constexpr int kThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
   const int kend = min(len, key0 + chunk);
   const int nkeys = max(0, kend - key0);
   const int T = (nkeys + kBN - 1) / kBN;
+  const int nsw = (p.G + 31) >> 5;  // softmax warps holding query rows (1..4)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -106,15 +109,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 32);
+      mbar_init(&bars->s_free[s], 32 * nsw);
     }
-    mbar_init(&bars->p_full, 32);
+    mbar_init(&bars->p_full, 32 * nsw);
     mbar_init(&bars->p_free, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 2) {
+  if (warp == 6) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 1) {
+  if (warp == 5) {
     // ------------------------------------------------------------ producer
     int* staged = reinterpret_cast<int*>(smem + kOffPages);
     const int page0 = PAGED ? key0 / p.block_size : 0;
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
           mbar_wait_drain(&bars->r_full[t % kRing], (t / kRing) & 1, 200000000ull);
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == 6) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && T > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, kBN, false, false);
@@ -250,9 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         mbar_wait_drain(&bars->drain, 0, 200000000ull);
       }
     }
-  } else {
-    // ------------------------------------------- softmax for rows 0..31, epilogue
-    const int row = lane;  // TMEM lane; rows < G are the group's query heads
+  } else if (warp < nsw) {
+    // ------------------------------- softmax for rows 32·warp … +31, epilogue
+    const int row = warp * 32 + lane;  // TMEM lane; rows < G are the group's query heads
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
-      const uint32_t sa = tmem + sb * kBN;
+      const uint32_t sa = tmem + lane_base + sb * kBN;
       tmem_ld32(sa + 0, r0);
       tmem_ld32(sa + 32, r1);
       tmem_ld32(sa + 64, r2);
@@ -321,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
           w0[e] = pack_bf16x2(s[2 * e], s[2 * e + 1]);
           w1[e] = pack_bf16x2(s[64 + 2 * e], s[64 + 2 * e + 1]);
         }
-        tmem_st32(tmem + sb * kBN, w0);
-        tmem_st32(tmem + sb * kBN + 32, w1);
+        tmem_st32(tmem + lane_base + sb * kBN, w0);
+        tmem_st32(tmem + lane_base + sb * kBN + 32, w1);
       }
       // Wait for P̃V(j−1) on every tile, not only before a rescale of O: the
       // final wait below tells phases apart by parity, which is only sound if
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t r[32];
-          const uint32_t oa = tmem + kColO + cc * 32;
+          const uint32_t oa = tmem + lane_base + kColO + cc * 32;
           tmem_ld32(oa, r);
           tmem_wait_ld();
           reg_fence(r);
@@ -344,8 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         }
       }
       tmem_wait_st();
-      if (PAGED && valid < kBN) {
-        // Zero the V rows past the sequence end once V_j has landed.
+      if (PAGED && valid < kBN && warp == 0) {
+        // Zero the V rows past the sequence end once V_j has landed (warp 0
+        // does it before its p_full arrival, which P̃V waits for).
         const int t = seq_v(j, T);
         ok = mbar_wait(&bars->r_full[t % kRing], (t / kRing) & 1, abort_flag, p.err, site(10));
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -378,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t r[32];
-          tmem_ld32(tmem + kColO + cc * 32, r);
+          tmem_ld32(tmem + lane_base + kColO + cc * 32, r);
           tmem_wait_ld();
           reg_fence(r);
           if (row < p.G) {
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 6) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -145,7 +145,7 @@ def test_gqa_decode_validates_before_cuda(L):
         return L.fa_decode_splitkv_gqa(FAKE, FAKE, FAKE, FAKE, None, 2, Hq, Hkv, 300, d, fa.FA_BF16, 0.1, 32, FAKE,
                                        wsb, None)
     assert dec(Hq=28, Hkv=5) == fa.FA_ERR_INVALID_ARG          # not a multiple
-    assert dec(Hq=132, Hkv=4) == fa.FA_ERR_UNSUPPORTED         # group of 33
+    assert dec(Hq=516, Hkv=4) == fa.FA_ERR_UNSUPPORTED         # group of 129
     assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
     assert dec(wsb=64) == fa.FA_ERR_INVALID_ARG
     assert b"workspace" in L.fa_get_last_error()
@@ -158,6 +158,7 @@ def test_paged_decode_validates_before_cuda(L):
     assert dec(bs=24) == fa.FA_ERR_UNSUPPORTED
     assert dec(bs=256) == fa.FA_ERR_UNSUPPORTED
     assert dec(Hq=30) == fa.FA_ERR_INVALID_ARG
+    assert dec(Hq=516) == fa.FA_ERR_UNSUPPORTED                # group of 129
     assert dec(table=None) == fa.FA_ERR_INVALID_ARG
     assert dec(wsb=16) == fa.FA_ERR_INVALID_ARG
     assert dec(d=64) == fa.FA_ERR_UNSUPPORTED

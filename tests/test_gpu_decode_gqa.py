@@ -52,6 +52,10 @@ def _run(seed, B, Hq, Hkv, N, splits, heads=None):
     (1, 4, 2, 20, 32),       # more splits than keys
     (2, 32, 2, 700, 4),      # group of 16
     (3, 32, 1, 1500, 8),     # multi-query attention: one key/value head for 32 query heads
+    (2, 48, 1, 900, 4),      # group of 48: two softmax warps, the second half full
+    (1, 71, 1, 1300, 8),     # group of 71: three softmax warps, a ragged last one
+    (2, 128, 2, 640, 4),     # group of 64
+    (1, 128, 1, 2000, 16),   # group of 128: all four TMEM lane quarters hold query rows
 ])
 def test_gqa_decode_matches_oracle(B, Hq, Hkv, N, splits):
     _run(31, B, Hq, Hkv, N, splits)

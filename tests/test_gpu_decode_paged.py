@@ -92,12 +92,14 @@ def _run(seed, B, Hq, Hkv, lens, bs, splits, heads=None):
     (1, 8, 2, [17000], 16, 1),               # 1063 pages in one split: past the 1024 staged page ids
     (2, 32, 1, [900, 333], 16, 4),           # multi-query attention over 16-key pages
     (2, 32, 2, [640, 129], 64, 2),           # groups of 16 over 64-key pages
+    (2, 64, 1, [900, 130], 16, 4),           # group of 64 (two softmax warps), partial last tiles
+    (1, 96, 2, [1000], 32, 2),               # groups of 48
 ])
 def test_paged_decode_matches_oracle(B, Hq, Hkv, lens, bs, splits):
     _run(41, B, Hq, Hkv, lens, bs, splits)
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4)])   # single-head kernel; grouped kernel's copy warps
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4)])   # single-head kernel; grouped tensor-core kernel
 def test_paged_decode_flags_a_bad_page_id_without_faulting(Hq, Hkv):
     import torch
     q, kc, vc, table, lens = _paged(42, 1, Hq, Hkv, [300], 16)
