@@ -79,7 +79,7 @@ def test_backward_writes_stay_inside_gradients_and_workspace(B, H, N, d, causal)
     _check(*grads, ws)
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (28, 4), (32, 1)])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (28, 4), (32, 1), (128, 2), (71, 1)])
 def test_decode_writes_stay_inside_output_and_workspace(Hq, Hkv):
     import torch
     B, N, S = 3, 777, 8
@@ -96,7 +96,7 @@ def test_decode_writes_stay_inside_output_and_workspace(Hq, Hkv):
     _check(o, lse, ws)
 
 
-@pytest.mark.parametrize("Hq,Hkv,bs", [(4, 4, 16), (28, 4, 16), (8, 2, 64), (32, 1, 32)])
+@pytest.mark.parametrize("Hq,Hkv,bs", [(4, 4, 16), (28, 4, 16), (8, 2, 64), (32, 1, 32), (96, 1, 16)])
 def test_paged_decode_writes_stay_inside_output_and_workspace(Hq, Hkv, bs):
     import torch
     B, S = 3, 4
