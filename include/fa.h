@@ -176,7 +176,7 @@ FA_API size_t fa_decode_workspace_size(int B, int H, int d, int n_splits);
  *   q [B,H,1,d], k and v [B,H,N_kv,d] contiguous; o [B,H,1,d]; lse [B,H] (or NULL).
  *   workspace: device buffer of at least fa_decode_workspace_size() bytes, used
  *   for the partial triples; its contents on entry do not matter.
- *   Supported: FA_BF16, d = 128, 1 ≤ n_splits ≤ 256.
+ *   Supported: FA_BF16, d = 64 or 128, 1 ≤ n_splits ≤ 256.
  */
 FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int N_kv, int d, fa_dtype dtype, float scale,
@@ -193,7 +193,7 @@ FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, 
  *   multiply-adds per key would outrun CUDA cores long before the HBM stream.
  *   q [B,H_q,1,d], k and v [B,H_kv,N_kv,d] contiguous; o [B,H_q,1,d]; lse [B,H_q]
  *   (or NULL).  workspace: fa_decode_workspace_size(B, H_q, d, n_splits) bytes.
- *   Supported: FA_BF16, d = 128, H_q = G·H_kv with 1 <= G <= 128 (G = H_q is
+ *   Supported: FA_BF16, d = 64 or 128, H_q = G·H_kv with 1 <= G <= 128 (G = H_q is
  *   multi-query attention), 1 ≤ n_splits ≤ 256.
  */
 FA_API fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -217,7 +217,7 @@ FA_API fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void*
  *   FA_ERR_INVALID_ARG.  Cache slots past a sequence's end may hold anything.
  *   q [B,H_q,1,d]; o [B,H_q,1,d]; lse [B,H_q] (or NULL); workspace as for
  *   fa_decode_splitkv with H = H_q.
- *   Supported: FA_BF16, d = 128, block_size ∈ {16, 32, 64, 128}, H_q = G·H_kv, G ≤ 128.
+ *   Supported: FA_BF16, d = 64 or 128, block_size ∈ {16, 32, 64, 128}, H_q = G·H_kv, G ≤ 128.
  */
 FA_API fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                                  const int32_t* seq_lens, void* o, float* lse, int B, int H_q, int H_kv,

@@ -511,8 +511,8 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
   if (B <= 0 || H <= 0 || N_kv <= 0 || d <= 0 || n_splits <= 0)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: sizes must be positive");
   if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: unknown dtype");
-  if (dtype != FA_BF16 || d != 128)
-    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv: only bf16 with d=128 is built");
+  if (dtype != FA_BF16 || (d != 64 && d != 128))
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv: only bf16 with d = 64 or 128 is built");
   if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv: n_splits must be <= 256");
   if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv: B and H must be <= 65535");
   if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv: scale must be finite and > 0");
@@ -536,6 +536,7 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
   p.H = H;
   p.Nkv = N_kv;
   p.n_splits = n_splits;
+  p.d = d;
   p.chunk = (N_kv + n_splits - 1) / n_splits;
   p.scale_log2 = scale * 1.4426950408889634f;
   fa_status r = watchdog_ptr(&p.err);
@@ -554,8 +555,8 @@ fa_status fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v,
     return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: sizes must be positive");
   if (dtype != FA_BF16 && dtype != FA_FP32)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: unknown dtype");
-  if (dtype != FA_BF16 || d != 128)
-    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_noalloc: only bf16 with d=128 is built");
+  if (dtype != FA_BF16 || (d != 64 && d != 128))
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_noalloc: only bf16 with d = 64 or 128 is built");
   if (n_splits > 256) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_noalloc: n_splits must be <= 256");
   if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_noalloc: B and H must be <= 65535");
   if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_noalloc: scale must be finite and > 0");
@@ -585,6 +586,7 @@ fa_status fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v,
   p.H = H;
   p.Nkv = N_kv;
   p.n_splits = n_splits;
+  p.d = d;
   p.chunk = (N_kv + n_splits - 1) / n_splits;
   p.scale_log2 = scale * 1.4426950408889634f;
   fa_status r = watchdog_ptr(&p.err);
@@ -603,8 +605,8 @@ fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, voi
   if (H_q % H_kv != 0)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
   if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_decode_splitkv_gqa: unknown dtype");
-  if (dtype != FA_BF16 || d != 128)
-    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: only bf16 with d=128 is built");
+  if (dtype != FA_BF16 || (d != 64 && d != 128))
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: only bf16 with d = 64 or 128 is built");
   if (H_q / H_kv > 128)  // the group's rows share one 128-row MMA tile
     return fail(FA_ERR_UNSUPPORTED, "fa_decode_splitkv_gqa: at most 128 query heads per key/value head (got %d)",
                 H_q / H_kv);
@@ -633,6 +635,7 @@ fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, voi
   p.G = H_q / H_kv;
   p.Nkv = N_kv;
   p.n_splits = n_splits;
+  p.d = d;
   p.chunk = (N_kv + n_splits - 1) / n_splits;
   p.scale_log2 = scale * 1.4426950408889634f;
   fa_status r = watchdog_ptr(&p.err);
@@ -659,6 +662,7 @@ fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, voi
   t.G = p.G;
   t.Nkv = N_kv;
   t.n_splits = n_splits;
+  t.d = d;
   t.chunk = p.chunk;
   t.scale_log2 = p.scale_log2;
   t.err = p.err;
@@ -681,7 +685,8 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
   if (H_q % H_kv != 0)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
   if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: unknown dtype");
-  if (dtype != FA_BF16 || d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: only bf16 with d=128 is built");
+  if (dtype != FA_BF16 || (d != 64 && d != 128))
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: only bf16 with d = 64 or 128 is built");
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
     return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: block_size must be 16, 32, 64 or 128 (got %d)", block_size);
   if (H_q / H_kv > 128)
@@ -712,6 +717,7 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
   p.H = H_q;
   p.Nkv = 0;
   p.n_splits = n_splits;
+  p.d = d;
   p.chunk = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.Hkv = H_kv;
@@ -743,8 +749,6 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
     return r;
   t.block_table = block_table;
   t.seq_lens = seq_lens;
-  t.k_pages = k_cache;
-  t.v_pages = v_cache;
   t.max_blocks = max_blocks;
   t.block_size = block_size;
   t.num_blocks = num_blocks;
@@ -756,6 +760,7 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
   t.G = p.G;
   t.Nkv = 0;
   t.n_splits = n_splits;
+  t.d = d;
   t.chunk = 0;
   t.scale_log2 = p.scale_log2;
   t.err = p.err;

@@ -21,19 +21,29 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 128;
 constexpr int kSub = 64;                      // keys per sub-chunk
-constexpr int kRowBytes = kD * 2;             // one bf16 key row
-constexpr int kStageBytes = 2 * kSub * kRowBytes;  // K then V: 32 KB
 constexpr int kThreads = 128;
-constexpr int kSmem = 2 * kStageBytes + 1024;
+
+// Sizes for head dim D (64 or 128).  A key's D values are spread over D/8
+// lanes (8 values each), so a warp covers 256/D keys at once, and the P·V sums
+// of the 4·256/D (warp, key slot) groups are combined at the end.
+template <int D>
+struct DecCfg {
+  static constexpr int kRowBytes = D * 2;                   // one bf16 key row
+  static constexpr int kStageBytes = 2 * kSub * kRowBytes;  // K then V
+  static constexpr int kSmem = 2 * kStageBytes + 1024;
+  static constexpr int kLanesPerKey = D / 8;
+  static constexpr int kKeysPerStep = 32 / kLanesPerKey;
+  static constexpr int kGroups = 4 * kKeysPerStep;
+  static_assert(kGroups * D == 1024, "partial sums fill the reduction buffer");
+};
 
 constexpr int kMaxStagedPages = 256;  // page ids of a CTA's key range held in shared memory
 
 struct DecodeSmem {
   float scores[kSub];
   float probs[kSub];
-  float red[8][kD];
+  float red[1024];  // [kGroups][D] partial P·V sums
   uint64_t full[2];
   int abort_flag;
   int pages[kMaxStagedPages];  // paged cache only: validated page ids of this CTA's range
@@ -65,18 +75,21 @@ __device__ __forceinline__ int checked_page(const DecodeParams& p, int b, int pa
 // bs, d], and how many rows of that page follow it.  `staged` holds the ids of
 // pages page0 … page0 + kMaxStagedPages − 1; later pages are read directly.
 __device__ __forceinline__ const uint8_t* paged_row(const void* cache, const DecodeParams& p, const int* staged,
-                                                    int page0, int b, int h, int t, int* piece_rows) {
+                                                    int page0, int b, int h, int t, int row_bytes, int* piece_rows) {
   const int page = t / p.block_size;
   const int slot = t - page * p.block_size;
   const int rel = page - page0;
   const int blk = rel < kMaxStagedPages ? staged[rel] : checked_page(p, b, page);
   *piece_rows = p.block_size - slot;
   return reinterpret_cast<const uint8_t*>(cache) +
-         ((static_cast<int64_t>(blk) * p.H + h) * p.block_size + slot) * kRowBytes;
+         ((static_cast<int64_t>(blk) * p.H + h) * p.block_size + slot) * row_bytes;
 }
 
-template <bool PAGED>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
+  using C = DecCfg<D>;
+  constexpr int kRowBytes = C::kRowBytes;
+  constexpr int kStageBytes = C::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
   uint8_t* ring = smem_raw + pad;
@@ -88,8 +101,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int dchunk = lane & 15;   // 8 head-dim values per lane
-  const int kpar = lane >> 4;     // which of the two keys a warp handles at once
+  const int dchunk = lane % C::kLanesPerKey;  // 8 head-dim values per lane
+  const int kpar = lane / C::kLanesPerKey;    // which of the warp's keys this lane works on
   const int64_t bh = static_cast<int64_t>(b) * p.H + h;
   int len = p.Nkv;
   int chunk = p.chunk;
@@ -143,8 +156,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
       const int r = lane * ps;
       if (r < n) {
         int rows;
-        const uint8_t* ksrc = paged_row(p.k, p, sm.pages, page0, b, h, key0 + i * kSub + r, &rows);
-        const uint8_t* vsrc = paged_row(p.v, p, sm.pages, page0, b, h, key0 + i * kSub + r, &rows);
+        const uint8_t* ksrc = paged_row(p.k, p, sm.pages, page0, b, h, key0 + i * kSub + r, kRowBytes, &rows);
+        const uint8_t* vsrc = paged_row(p.v, p, sm.pages, page0, b, h, key0 + i * kSub + r, kRowBytes, &rows);
         rows = min(min(rows, ps), n - r);
         bulk_load(ring + st * kStageBytes + r * kRowBytes, ksrc, rows * kRowBytes, &sm.full[st]);
         bulk_load(ring + st * kStageBytes + kSub * kRowBytes + r * kRowBytes, vsrc, rows * kRowBytes, &sm.full[st]);
@@ -179,17 +192,17 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     const uint8_t* sK = ring + st * kStageBytes;
     const uint8_t* sV = sK + kSub * kRowBytes;
 
-    // Scores: each warp takes 16 keys, two at a time (one per half-warp).
+    // Scores: each warp takes 16 keys, kKeysPerStep at a time.
 #pragma unroll
-    for (int pr = 0; pr < 8; ++pr) {
-      const int key = warp * 16 + pr * 2 + kpar;
+    for (int pr = 0; pr < 16 / C::kKeysPerStep; ++pr) {
+      const int key = warp * 16 + pr * C::kKeysPerStep + kpar;
       float kf[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + key * kRowBytes + dchunk * 16), kf);
       float dot = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) dot = fmaf(qf[e], kf[e], dot);
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      for (int o = C::kLanesPerKey / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
       if (dchunk == 0) sm.scores[key] = (key < n) ? dot * sl2 : -INFINITY;
     }
     __syncthreads();
@@ -215,12 +228,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     }
     __syncthreads();
 
-    // P·V: lane owns 8 head-dim values; the 8 (warp, half) groups split the keys.
+    // P·V: lane owns 8 head-dim values; the kGroups (warp, key slot) groups split the keys.
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] *= corr;
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-      const int key = ii * 8 + warp * 2 + kpar;
+    for (int ii = 0; ii < kSub / C::kGroups; ++ii) {
+      const int key = ii * C::kGroups + warp * C::kKeysPerStep + kpar;
       if (key < n) {
         const float pk = sm.probs[key];
         float vf[8];
@@ -242,27 +255,30 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     return;
   }
 
-  // Combine the 8 key groups, then write the unnormalised triple.
-  const int g = warp * 2 + kpar;
+  // Combine the key groups, then write the unnormalised triple.
+  const int g = warp * C::kKeysPerStep + kpar;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) sm.red[g][dchunk * 8 + e] = acc[e];
+  for (int e = 0; e < 8; ++e) sm.red[g * D + dchunk * 8 + e] = acc[e];
   __syncthreads();
-  float o = 0.f;
-#pragma unroll
-  for (int gg = 0; gg < 8; ++gg) o += sm.red[gg][tid];
   const int64_t slot = bh * p.n_splits + c;
-  p.part_o[slot * kD + tid] = o;
+  if (tid < D) {
+    float o = 0.f;
+#pragma unroll
+    for (int gg = 0; gg < C::kGroups; ++gg) o += sm.red[gg * D + tid];
+    p.part_o[slot * D + tid] = o;
+  }
   if (tid == 0) {
     p.part_ml[slot * 2 + 0] = m_run;  // −∞ and ℓ = 0 for a split with no keys
     p.part_ml[slot * 2 + 1] = l_run;
   }
 }
 
-__global__ void __launch_bounds__(kD) decode_merge_kernel(const DecodeParams p) {
+template <int D>
+__global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
   const int64_t bh = blockIdx.x;
   const int t = threadIdx.x;
   const float* ml = p.part_ml + bh * p.n_splits * 2;
-  const float* po = p.part_o + bh * p.n_splits * kD;
+  const float* po = p.part_o + bh * p.n_splits * D;
   float m = -INFINITY;
   for (int c = 0; c < p.n_splits; ++c) m = fmaxf(m, ml[2 * c]);
   float l = 0.f, o = 0.f;
@@ -270,39 +286,48 @@ __global__ void __launch_bounds__(kD) decode_merge_kernel(const DecodeParams p) 
     const float mc = ml[2 * c];
     const float w = (mc == -INFINITY) ? 0.f : ex2_approx(mc - m);
     l = fmaf(ml[2 * c + 1], w, l);
-    o = fmaf(po[static_cast<int64_t>(c) * kD + t], w, o);
+    o = fmaf(po[static_cast<int64_t>(c) * D + t], w, o);
   }
-  reinterpret_cast<__nv_bfloat16*>(p.o)[bh * kD + t] = __float2bfloat16_rn(o / l);
+  reinterpret_cast<__nv_bfloat16*>(p.o)[bh * D + t] = __float2bfloat16_rn(o / l);
   if (t == 0 && p.lse != nullptr) p.lse[bh] = (m + __log2f(l)) * 0.69314718055994531f;
+}
+
+template <int D, bool PAGED>
+cudaError_t launch_split(const DecodeParams& p, cudaStream_t stream) {
+  constexpr int kSmem = DecCfg<D>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<D, PAGED><<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<D><<<p.B * p.H, D, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode_paged_bf16(const DecodeParams& p, cudaStream_t stream) {
   if (p.G != 1) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
-  decode_split_kernel<true><<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (p.d == 128) return launch_split<128, true>(p, stream);
+  if (p.d == 64) return launch_split<64, true>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
-  decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
+  if (p.d == 128)
+    decode_merge_kernel<128><<<p.B * p.H, 128, 0, stream>>>(p);
+  else if (p.d == 64)
+    decode_merge_kernel<64><<<p.B * p.H, 64, 0, stream>>>(p);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t stream) {
-  if (d != kD || p.G != 1) return cudaErrorInvalidValue;  // groups go to the tensor-core kernel
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
-  decode_split_kernel<false><<<dim3(p.n_splits, p.H, p.B), kThreads, kSmem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  decode_merge_kernel<<<p.B * p.H, kD, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (p.G != 1 || d != p.d) return cudaErrorInvalidValue;  // groups go to the tensor-core kernel
+  if (d == 128) return launch_split<128, false>(p, stream);
+  if (d == 64) return launch_split<64, false>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

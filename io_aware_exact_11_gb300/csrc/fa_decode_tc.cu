@@ -42,23 +42,32 @@ namespace {
 
 constexpr int kBN = 128;
 constexpr int kTileBytes = 128 * 128;    // [128 rows][64 bf16], 128-byte swizzle
-constexpr int kSlot = 2 * kTileBytes;    // one 128 × 128 bf16 tile
-constexpr int kRing = 5;
 constexpr int kThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
-
-constexpr int kOffQ = 0;
-constexpr int kOffR = kOffQ + kSlot;
-constexpr int kOffPages = kOffR + kRing * kSlot;  // paged cache: staged page ids
 constexpr int kMaxStagedPages = 1024;
-constexpr int kOffBar = kOffPages + kMaxStagedPages * 4;
-constexpr int kSmem = kOffBar + 256 + 1024;
+constexpr int kMaxRing = 10;
+
+// Shared-memory layout for head dim D: a Q, K or V tile is D/64 swizzled
+// [128 rows][64 columns] blocks; the ring holds about 160 KB of K/V tiles
+// (5 slots at d = 128, 10 at d = 64), which keeps enough copies in flight.
+template <int D>
+struct TcCfg {
+  static constexpr int kNKB = D / 64;
+  static constexpr int kSlot = kNKB * kTileBytes;
+  static constexpr int kRing = D == 64 ? 10 : 5;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffR = kOffQ + kSlot;
+  static constexpr int kOffPages = kOffR + kRing * kSlot;  // paged cache: staged page ids
+  static constexpr int kOffBar = kOffPages + kMaxStagedPages * 4;
+  static constexpr int kSmem = kOffBar + 256 + 1024;
+  static_assert(kRing <= kMaxRing, "ring barriers");
+};
 
 struct Bars {
   uint64_t q_full;
-  uint64_t r_full[kRing], r_empty[kRing];
+  uint64_t r_full[kMaxRing], r_empty[kMaxRing];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, p_free;
   uint64_t drain;
@@ -71,12 +80,14 @@ __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernDeco
 __device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int seq_v(int j, int T) { return min(2 * j + 2, 2 * T - 1); }
 
-template <bool PAGED>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid_constant__ DecodeTcParams p) {
+  using C = TcCfg<D>;
+  constexpr int kSlot = C::kSlot, kRing = C::kRing, kOffQ = C::kOffQ, kOffR = C::kOffR;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -128,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
 
   if (warp == 5) {
     // ------------------------------------------------------------ producer
-    int* staged = reinterpret_cast<int*>(smem + kOffPages);
+    int* staged = reinterpret_cast<int*>(smem + C::kOffPages);
     const int page0 = PAGED ? key0 / p.block_size : 0;
     if (PAGED && T > 0) {
       // The warp stages this range's page ids with one coalesced, checked load.
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
         mbar_arrive_expect_tx(&bars->q_full, kSlot);
-        for (int kb = 0; kb < 2; ++kb)
+        for (int kb = 0; kb < C::kNKB; ++kb)
           tma_load_4d(smem + kOffQ + kb * kTileBytes, &p.tm_q, &bars->q_full, kb * 64, qrow0, 0, 0);
       }
       int issued = 0;
@@ -180,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         __syncwarp();
         const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
         if (!PAGED) {
-          if (lane < 2)
+          if (lane < C::kNKB)
             tma_load_4d(smem + kOffR + slot * kSlot + lane * kTileBytes, tm, &bars->r_full[slot], lane * 64,
                         key0 + jt * kBN, hkv, b);
         } else {
@@ -192,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
               blk = page_id(t0);
             else
               row = bs;  // wholly out of range: zero fill
-            for (int kb = 0; kb < 2; ++kb)
+            for (int kb = 0; kb < C::kNKB; ++kb)
               tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes + lane * bs * 128, tm,
                           &bars->r_full[slot], kb * 64, row, hkv, blk);
           }
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && T > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, kBN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, false, true);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
       const uint32_t sQ = smem_u32(smem + kOffQ);
       const uint32_t sR = smem_u32(smem + kOffR);
       auto issue_pv = [&](int jj) -> bool {
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         tc_fence_after();
         const uint32_t kb = sR + slot * kSlot;
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
           mma_bf16_ss(tmem + sb * kBN, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescS,
                       kk > 0 ? 1u : 0u);
@@ -336,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t r[32];
           const uint32_t oa = tmem + lane_base + kColO + cc * 32;
           tmem_ld32(oa, r);
@@ -357,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         uint8_t* vt = smem + kOffR + (t % kRing) * kSlot;
         for (int rr = max(valid, 0) + lane; rr < kBN; rr += 32)
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb)
+          for (int kb = 0; kb < C::kNKB; ++kb)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               *reinterpret_cast<uint4*>(vt + kb * kTileBytes + rr * 128 + q * 16) = make_uint4(0, 0, 0, 0);
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
     if (T == 0) {
       if (row < p.G) {
         const int64_t slot = static_cast<int64_t>(qrow0 + row) * p.n_splits + c;
-        for (int e = 0; e < 128; ++e) p.part_o[slot * 128 + e] = 0.f;
+        for (int e = 0; e < D; ++e) p.part_o[slot * D + e] = 0.f;
         p.part_ml[slot * 2 + 0] = -INFINITY;
         p.part_ml[slot * 2 + 1] = 0.f;
       }
@@ -381,13 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         tc_fence_after();
         const int64_t slot = static_cast<int64_t>(qrow0 + row) * p.n_splits + c;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + kColO + cc * 32, r);
           tmem_wait_ld();
           reg_fence(r);
           if (row < p.G) {
-            float4* dst = reinterpret_cast<float4*>(p.part_o + slot * 128 + cc * 32);
+            float4* dst = reinterpret_cast<float4*>(p.part_o + slot * D + cc * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
               dst[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
@@ -410,12 +421,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
   }
 }
 
+template <int D, bool PAGED>
+cudaError_t launch_gqa_d(const DecodeTcParams& p, cudaStream_t stream) {
+  constexpr int kSmem = TcCfg<D>::kSmem;
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_gqa_tc_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_gqa_tc_kernel<D, PAGED><<<dim3(p.n_splits, p.Hkv, p.B), kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <bool PAGED>
 cudaError_t launch_gqa(const DecodeTcParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_gqa_tc_kernel<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
-  decode_gqa_tc_kernel<PAGED><<<dim3(p.n_splits, p.Hkv, p.B), kThreads, kSmem, stream>>>(p);
-  return cudaGetLastError();
+  if (p.d == 128) return launch_gqa_d<128, PAGED>(p, stream);
+  if (p.d == 64) return launch_gqa_d<64, PAGED>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace

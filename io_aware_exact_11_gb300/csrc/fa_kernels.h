@@ -59,6 +59,7 @@ struct DecodeParams {
   const int* block_table = nullptr;  // [B, max_blocks]
   const int* seq_lens = nullptr;     // [B]
   int max_blocks = 0, block_size = 0, num_blocks = 0;
+  int d = 128;  // head dim: 64 or 128
 };
 
 // Device-side argument checks report through the status word with these sites.
@@ -71,12 +72,11 @@ struct DecodeTcParams {
   CUtensorMap tm_v;
   const int* block_table;  // paged cache only: [B, max_blocks]
   const int* seq_lens;     // paged cache only: [B]
-  const void* k_pages;     // paged cache only: [num_blocks, Hkv, bs, d] bf16 (copied per thread for small pages)
-  const void* v_pages;
   int max_blocks, block_size, num_blocks;
   float* part_o;     // [B,Hq,S,d] fp32
   float* part_ml;    // [B,Hq,S,2] fp32
   int B, Hq, Hkv, G, Nkv, n_splits, chunk;
+  int d;             // head dim: 64 or 128
   float scale_log2;
   unsigned int* err;
 };

@@ -99,7 +99,7 @@ def test_decode_rejects_bad_arguments(L):
     assert dec(ws=None) == fa.FA_ERR_INVALID_ARG
     assert dec(wsb=100) == fa.FA_ERR_INVALID_ARG
     assert b"workspace" in L.fa_get_last_error()
-    assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert dec(d=96) == fa.FA_ERR_UNSUPPORTED
     assert dec(dt=fa.FA_FP32) == fa.FA_ERR_UNSUPPORTED
     assert dec(ns=0) == fa.FA_ERR_INVALID_ARG
     assert dec(ns=257) == fa.FA_ERR_UNSUPPORTED
@@ -146,7 +146,7 @@ def test_gqa_decode_validates_before_cuda(L):
                                        wsb, None)
     assert dec(Hq=28, Hkv=5) == fa.FA_ERR_INVALID_ARG          # not a multiple
     assert dec(Hq=516, Hkv=4) == fa.FA_ERR_UNSUPPORTED         # group of 129
-    assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert dec(d=96) == fa.FA_ERR_UNSUPPORTED
     assert dec(wsb=64) == fa.FA_ERR_INVALID_ARG
     assert b"workspace" in L.fa_get_last_error()
 
@@ -161,7 +161,7 @@ def test_paged_decode_validates_before_cuda(L):
     assert dec(Hq=516) == fa.FA_ERR_UNSUPPORTED                # group of 129
     assert dec(table=None) == fa.FA_ERR_INVALID_ARG
     assert dec(wsb=16) == fa.FA_ERR_INVALID_ARG
-    assert dec(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert dec(d=96) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_host_forward_workspace_size(L):

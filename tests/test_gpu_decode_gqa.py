@@ -27,8 +27,7 @@ def _lib():
     fa.device_status()
 
 
-def _run(seed, B, Hq, Hkv, N, splits, heads=None):
-    d = 128
+def _run(seed, B, Hq, Hkv, N, splits, heads=None, d=128):
     hq = inputs.normal_tensor(seed, "q", B, Hq, 1, d, "bf16")
     hk = inputs.normal_tensor(seed, "k", B, Hkv, N, d, "bf16")
     hv = inputs.normal_tensor(seed, "v", B, Hkv, N, d, "bf16")
@@ -59,6 +58,12 @@ def _run(seed, B, Hq, Hkv, N, splits, heads=None):
 ])
 def test_gqa_decode_matches_oracle(B, Hq, Hkv, N, splits):
     _run(31, B, Hq, Hkv, N, splits)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,splits", [(2, 28, 4, 1000, 32), (1, 64, 1, 1300, 8), (2, 6, 3, 777, 7)])
+def test_gqa_decode_head_dim_64_matches_oracle(B, Hq, Hkv, N, splits):
+    """d = 64: one 64-column block per tile, a ten-slot ring, N = 64 for P̃V."""
+    _run(32, B, Hq, Hkv, N, splits, d=64)
 
 
 def test_gqa_decode_with_group_one_equals_decode():

@@ -31,9 +31,8 @@ def _lib():
     fa.device_status()
 
 
-def _paged(seed, B, Hq, Hkv, lens, bs, extra_pages=5):
+def _paged(seed, B, Hq, Hkv, lens, bs, extra_pages=5, d=128):
     """Seeded contiguous K/V scattered into a shuffled, NaN-filled page pool."""
-    d = 128
     maxlen = int(max(lens))
     per = -(-maxlen // bs)
     k = inputs.normal_tensor(seed, "k", B, Hkv, maxlen, d, "bf16")
@@ -57,10 +56,10 @@ def _paged(seed, B, Hq, Hkv, lens, bs, extra_pages=5):
     return q, kc, vc, table, np.asarray(lens, dtype=np.int32)
 
 
-def _run(seed, B, Hq, Hkv, lens, bs, splits, heads=None):
+def _run(seed, B, Hq, Hkv, lens, bs, splits, heads=None, d=128):
     import torch
-    q, kc, vc, table, lens = _paged(seed, B, Hq, Hkv, lens, bs)
-    scale = 1 / math.sqrt(128)
+    q, kc, vc, table, lens = _paged(seed, B, Hq, Hkv, lens, bs, d=d)
+    scale = 1 / math.sqrt(d)
     qd = to_device(q[:, :, None, :].copy(), "bf16")
     o, lse = fa.decode_paged(qd, to_device(kc, "bf16"), to_device(vc, "bf16"), torch.from_numpy(table).cuda(),
                              torch.from_numpy(lens).cuda(), n_splits=splits, scale=scale)
@@ -97,6 +96,15 @@ def _run(seed, B, Hq, Hkv, lens, bs, splits, heads=None):
 ])
 def test_paged_decode_matches_oracle(B, Hq, Hkv, lens, bs, splits):
     _run(41, B, Hq, Hkv, lens, bs, splits)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,lens,bs,splits", [
+    (3, 4, 4, [1000, 37, 2049], 16, 8),      # single-head kernel
+    (3, 28, 4, [1000, 1, 300], 16, 4),       # grouped kernel, partial last tiles
+    (2, 64, 1, [700, 130], 64, 2),           # group of 64
+])
+def test_paged_decode_head_dim_64_matches_oracle(B, Hq, Hkv, lens, bs, splits):
+    _run(42, B, Hq, Hkv, lens, bs, splits, d=64)
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4)])   # single-head kernel; grouped tensor-core kernel

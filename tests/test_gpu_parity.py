@@ -178,8 +178,7 @@ def test_long_context_sampled_and_linear_memory():
 # ----------------------------------------------------------------- decode
 
 
-def _decode_check(seed, B, H, N, n_splits, heads=None):
-    d = 128
+def _decode_check(seed, B, H, N, n_splits, heads=None, d=128):
     host, dev = make_qkv(seed, B, H, 1, N, d, "bf16")
     scale = 1 / math.sqrt(d)
     o, lse = fa.decode_splitkv(dev["q"], dev["k"], dev["v"], n_splits=n_splits, scale=scale)
@@ -197,6 +196,12 @@ def _decode_check(seed, B, H, N, n_splits, heads=None):
                                           (1, 2, 20, 32), (1, 1, 1, 4), (1, 1, 4096, 256)])
 def test_decode_matches_oracle(B, H, N, splits):
     _decode_check(3, B, H, N, splits)
+
+
+@pytest.mark.parametrize("B,H,N,splits", [(2, 3, 1000, 32), (1, 2, 777, 7), (1, 1, 1, 4)])
+def test_decode_head_dim_64_matches_oracle(B, H, N, splits):
+    """d = 64: eight lanes per key, four keys per warp step, sixteen P·V groups."""
+    _decode_check(4, B, H, N, splits, d=64)
 
 
 def test_decode_matches_forward_kernel():
