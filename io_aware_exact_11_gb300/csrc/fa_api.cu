@@ -204,6 +204,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     if ((r = make_map(&p.tm_q, q, B, H, N_q, d, st[0], st[1], st[2], "q")) != FA_OK) return r;
     if ((r = make_map(&p.tm_k, k, B, H, N_kv, d, st[3], st[4], st[5], "k")) != FA_OK) return r;
     if ((r = make_map(&p.tm_v, v, B, H, N_kv, d, st[6], st[7], st[8], "v")) != FA_OK) return r;
+    if ((r = make_map(&p.tm_o, o, B, H, N_q, d, st[9], st[10], st[11], "o")) != FA_OK) return r;
     if ((r = watchdog_ptr(&p.err)) != FA_OK) return r;
     p.o = o;
     p.lse = lse;
@@ -287,6 +288,7 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, f
   if ((r = make_map(&p.tm_q, q, B, H, N_q, d, H * nq, nq, d, "q", 128, true)) != FA_OK) return r;
   if ((r = make_map(&p.tm_k, k, B, H, N_kv, d, H * nk, nk, d, "k", 128, true)) != FA_OK) return r;
   if ((r = make_map(&p.tm_v, v, B, H, N_kv, d, H * nk, nk, d, "v", 128, true)) != FA_OK) return r;
+  if ((r = make_map(&p.tm_o, o, B, H, N_q, d, H * nq, nq, d, "o")) != FA_OK) return r;
   if ((r = watchdog_ptr(&p.err)) != FA_OK) return r;
   p.o = o;
   p.lse = lse;

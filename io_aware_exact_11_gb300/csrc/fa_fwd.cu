@@ -35,6 +35,11 @@
 //   warps 2..5   softmax / rescale / epilogue of Q_0 (warp w reads TMEM lanes 32·(w%4)…)
 //   warps 6..9   the same for Q_1
 // TMEM: S_0 / P̃_0 (columns 0..127), S_1 / P̃_1 (128..255), O_0 (256..), O_1 (384..).
+// Epilogue: each softmax thread writes its row of O/ℓ (bf16) into 128-byte-
+// swizzled blocks in ring slots that no MMA still reads, and one thread per
+// query tile stores the blocks with TMA, so O leaves in full lines instead of
+// one 16-byte piece of 32 different rows per warp store (d = 64 keeps the
+// direct stores, which measured faster there).
 // Shared memory holds Q, K, V in the 128-byte-swizzled layout TMA writes:
 // blocks of [128 rows][128 bytes].
 //
@@ -100,6 +105,17 @@ struct FwdBars {
 };
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernFwd << 8) | s; }
+
+// TMA store of one box from shared memory (bulk-group completion), and the
+// wait until the group's shared-memory sources have been read.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Four fp32 values -> four E4M3 bytes (round to nearest even, saturating), the
 // first value in the lowest byte.
@@ -385,34 +401,92 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       mbar_arrive(&bars->p_full[qt]);
       m_run = m_new;
     }
-    if (ok) {
-      ok = W::wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
-      if (__all_sync(0xffffffffu, ok)) {
+    if constexpr (D == 64) {
+      // Head dim 64: each thread writes its 128-byte row directly (measured
+      // faster here than staging through shared memory).
+      if (ok) {
+        ok = W::wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
+        if (__all_sync(0xffffffffu, ok)) {
+          tc_fence_after();
+          const float inv = p.o_scale / l_run;
+          const int grow = m0 + qt * kBM + row;
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + b * p.o_sb + h * p.o_sh +
+                                static_cast<int64_t>(grow) * p.o_sn;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + o_col + c * 32, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            if (grow < p.Nq) {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * inv, __uint_as_float(r[8 * q4 + 1]) * inv);
+                v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * inv, __uint_as_float(r[8 * q4 + 3]) * inv);
+                v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * inv, __uint_as_float(r[8 * q4 + 5]) * inv);
+                v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * inv, __uint_as_float(r[8 * q4 + 7]) * inv);
+                *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = v;
+              }
+            }
+          }
+          if (p.lse != nullptr && grow < p.Nq)
+            p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + grow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        }
+      }
+    } else {
+      // O goes out through shared memory and TMA: the ring slots are idle once
+      // O is complete.  Each thread writes its row into 128-byte-swizzled
+      // [128 rows][64 columns] blocks, then one thread stores the blocks.  Every
+      // warp of the warpgroup reaches the barrier once, even after an abort (the
+      // store is then skipped), so none waits for a warp that left.
+      bool eok = false;
+      if (ok) {
+        ok = W::wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
+        eok = __all_sync(0xffffffffu, ok);
+      }
+      const int grow = m0 + qt * kBM + row;
+      // Staging blocks go to the ring slots the next loads would have used,
+      // (2T + n) mod kRing: those last held K/V tiles of key tile T−3 or earlier,
+      // which every issued MMA has finished with, and at most 4 < kRing slots are
+      // taken, so they never reach slot (2T−1) mod kRing, whose V tile the other
+      // query tile's last P̃V may still be reading.
+      constexpr int kBps = L::kSlot / kTileBytes;  // 16 KB blocks per ring slot
+      auto stage_block = [&](int n) -> uint8_t* {    // n = qt·(D/64) + kb
+        return smem + L::kR + ((2 * T + n / kBps) % L::kRing) * L::kSlot + (n % kBps) * kTileBytes;
+      };
+      static_assert(kQT * (D / 64) / (L::kSlot / kTileBytes) + 1 <= L::kRing, "staging slots");
+      if (eok) {
         tc_fence_after();
         const float inv = p.o_scale / l_run;
-        const int grow = m0 + qt * kBM + row;
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + b * p.o_sb + h * p.o_sh +
-                              static_cast<int64_t>(grow) * p.o_sn;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + o_col + c * 32, r);
           tmem_wait_ld();
           reg_fence(r);
-          if (grow < p.Nq) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * inv, __uint_as_float(r[8 * q4 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * inv, __uint_as_float(r[8 * q4 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * inv, __uint_as_float(r[8 * q4 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * inv, __uint_as_float(r[8 * q4 + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = v;
-            }
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * inv, __uint_as_float(r[8 * q4 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * inv, __uint_as_float(r[8 * q4 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * inv, __uint_as_float(r[8 * q4 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * inv, __uint_as_float(r[8 * q4 + 7]) * inv);
+            const int ch = c * 4 + q4;  // 16-byte chunk of the row
+            *reinterpret_cast<uint4*>(stage_block(qt * (D / 64) + (ch >> 3)) + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
+                v;
           }
         }
         if (p.lse != nullptr && grow < p.Nq)
           p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + grow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      }
+      fence_proxy_async_smem();
+      named_sync(1 + qt, 128);
+      if (wq == 0 && lane == 0 && !*abort_flag && m0 + qt * kBM < p.Nq) {  // rows past N_q are clipped
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_store_4d(&p.tm_o, stage_block(qt * (D / 64) + kb), kb * 64, m0 + qt * kBM, h, b);
+        bulk_commit();
+        bulk_wait_read();  // the source must stay until read; the writes complete with the grid
       }
     }
   }

@@ -28,6 +28,7 @@ struct FwdParams {
   int causal;                // query i sees keys j <= i + (Nkv − Nq); needs Nq <= Nkv
   unsigned int* err;
   float o_scale = 1.f;       // multiplies O before the 1/ℓ (FP8: the V descale factor)
+  CUtensorMap tm_o;          // O as {d, N_q, H, B} (its strides), box {64, 128, 1, 1}, 128-byte swizzle
 };
 
 struct FwdF32Params {
