@@ -44,12 +44,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
-    "fwd_prefill": {"src": "a69cf3aef1d92cc7", "bytes": 402752768 + 122092544},
+    "fwd_prefill": {"src": "691ff72798141c79", "bytes": 402787072 + 121707008},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
-    "bwd_train": {"src": "bc65c6763634f1bb", "bytes": 404855808 + 217765376},
+    "bwd_train": {"src": "76efbd405334fe22", "bytes": 404883200 + 222745088},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
     # proportional to B, stored here scaled to the B=64 launch
-    "decode_split": {"src": "913ed3c674a4d11b", "bytes": (1073859584 + 6917120) * 8},
+    "decode_split": {"src": "01d15147b0d37913", "bytes": (1073837056 + 6951168) * 8},
 }
 
 

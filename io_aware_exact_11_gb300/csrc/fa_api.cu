@@ -810,6 +810,8 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   if ((r = make_map(&p.tm_k, k, B, H, N, d, H * nd, nd, d, "k")) != FA_OK) return r;
   if ((r = make_map(&p.tm_v, v, B, H, N, d, H * nd, nd, d, "v")) != FA_OK) return r;
   if ((r = make_map(&p.tm_do, dout, B, H, N, d, H * nd, nd, d, "dout")) != FA_OK) return r;
+  if ((r = make_map(&p.tm_dk, dk, B, H, N, d, H * nd, nd, d, "dk")) != FA_OK) return r;
+  if ((r = make_map(&p.tm_dv, dv, B, H, N, d, H * nd, nd, d, "dv")) != FA_OK) return r;
   if ((r = watchdog_ptr(&p.err)) != FA_OK) return r;
   const size_t rows = static_cast<size_t>(B) * H * N;
   char* ws = static_cast<char*>(workspace);

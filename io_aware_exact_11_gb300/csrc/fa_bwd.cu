@@ -163,19 +163,6 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BwdParams p) 
   }
 }
 
-// Writes one 128-value bf16 row segment of 32 values (4 × 16 bytes) from fp32.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul) {
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    uint4 v;
-    v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * mul, __uint_as_float(r[8 * q4 + 1]) * mul);
-    v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * mul, __uint_as_float(r[8 * q4 + 3]) * mul);
-    v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * mul, __uint_as_float(r[8 * q4 + 5]) * mul);
-    v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * mul, __uint_as_float(r[8 * q4 + 7]) * mul);
-    *reinterpret_cast<uint4*>(dst + q4 * 8) = v;
-  }
-}
-
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -462,24 +449,47 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       tc_fence_before();
       mbar_arrive(&bars->ds_ready);
     }
+    // Warpgroup 0 writes dV, warpgroup 1 dK (with σ), through shared memory and
+    // TMA: once every MMA is complete (acc_done) the Q buffers are free.  Each
+    // thread writes its key row into 128-byte-swizzled [128 rows][64 columns]
+    // blocks and one thread per warpgroup stores them (rows past N are clipped).
+    // Every warp reaches the barrier once, even after an abort (the store is
+    // then skipped).
+    bool eok = false;
     if (ok) {
       ok = mbar_wait(&bars->acc_done, 0, abort_flag, p.err, site(11));
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        // Warpgroup 0 writes dV, warpgroup 1 dK (with σ).
-        const int64_t grow = bh * p.N + static_cast<int64_t>(j) * kTile + r;
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(cw == 0 ? p.dv : p.dk) + grow * D;
-        const uint32_t col = cw == 0 ? kColDV : kColDK;
-        const float mul = cw == 0 ? 1.f : p.scale;
+      eok = __all_sync(0xffffffffu, ok);
+    }
+    uint8_t* ob = smem + kOffQ + cw * (D / 64) * kTileBytes;
+    if (eok) {
+      tc_fence_after();
+      const uint32_t col = cw == 0 ? kColDV : kColDK;
+      const float mul = cw == 0 ? 1.f : p.scale;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + col + cc * 32, rr);
-          tmem_wait_ld();
-          reg_fence(rr);
-          if (!key_pad) store_row32(out + cc * 32, rr, mul);
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + col + cc * 32, rr);
+        tmem_wait_ld();
+        reg_fence(rr);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(rr[8 * q4 + 0]) * mul, __uint_as_float(rr[8 * q4 + 1]) * mul);
+          v.y = pack_bf16x2(__uint_as_float(rr[8 * q4 + 2]) * mul, __uint_as_float(rr[8 * q4 + 3]) * mul);
+          v.z = pack_bf16x2(__uint_as_float(rr[8 * q4 + 4]) * mul, __uint_as_float(rr[8 * q4 + 5]) * mul);
+          v.w = pack_bf16x2(__uint_as_float(rr[8 * q4 + 6]) * mul, __uint_as_float(rr[8 * q4 + 7]) * mul);
+          const int ch = cc * 4 + q4;  // 16-byte chunk of the row
+          *reinterpret_cast<uint4*>(ob + (ch >> 3) * kTileBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
         }
       }
+    }
+    fence_proxy_async_smem();
+    named_sync(bar_id, 128);
+    if (wq == 0 && lane == 0 && !*abort_flag) {
+      const CUtensorMap* map = cw == 0 ? &p.tm_dv : &p.tm_dk;
+      for (int kb = 0; kb < D / 64; ++kb) tma_store_4d(map, ob + kb * kTileBytes, kb * 64, j * kTile, h, b);
+      bulk_commit();
+      bulk_wait_read();  // the source must stay until read; the writes complete with the grid
     }
     tc_fence_before();
     named_sync(2, kThreads);

@@ -106,17 +106,6 @@ struct FwdBars {
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernFwd << 8) | s; }
 
-// TMA store of one box from shared memory (bulk-group completion), and the
-// wait until the group's shared-memory sources have been read.
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
-                                             int c3) {
-  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
 // Four fp32 values -> four E4M3 bytes (round to nearest even, saturating), the
 // first value in the lowest byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {

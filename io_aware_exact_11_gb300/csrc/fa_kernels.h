@@ -102,6 +102,8 @@ struct BwdParams {
   float scale_log2;   // σ·log2(e)
   int causal;         // key j visible to query i when j <= i
   unsigned int* err;
+  CUtensorMap tm_dk;  // dK, dV as {d, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle (TMA stores)
+  CUtensorMap tm_dv;
 };
 
 cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t s);
