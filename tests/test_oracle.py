@@ -121,6 +121,17 @@ def test_single_key_returns_its_value_and_score():
     assert np.allclose(lse, 1.3 * (q @ k[0]), atol=1e-15)
 
 
+def test_head_dim_one_by_hand():
+    """d = 1, σ = 1: q = ln 2, keys (1, 0) give scores (ln 2, 0), softmax weights (2/3, 1/3); with values
+    (3, 6) the output is 2/3·3 + 1/3·6 = 4 and LSE = ln(2 + 1) = ln 3."""
+    q = np.array([[math.log(2.0)]])
+    k = np.array([[1.0], [0.0]])
+    v = np.array([[3.0], [6.0]])
+    o, lse = oracle.attention_forward(q, k, v, 1.0)
+    assert abs(o[0, 0] - 4.0) <= 1e-14
+    assert abs(lse[0] - math.log(3.0)) <= 1e-14
+
+
 def test_large_scores_are_stable():
     q = RNG.standard_normal((4, 8)) * 40
     k = RNG.standard_normal((20, 8)) * 40
