@@ -137,7 +137,11 @@ FA_API size_t fa_forward_host_workspace_size(int B, int H, int N_q, int N_kv, in
  *   streams and `stream`, ordered after the work already queued on `stream`.
  *   The call returns once everything is queued; o and lse are valid after
  *   `stream` has been synchronised.  Results equal fa_forward_masked's on the
- *   same data.  Calls on one device are serialised internally.  Argument errors
+ *   same data.  Calls on one device are serialised internally: outside graph
+ *   capture, a call's first copy in waits until the previous call has copied
+ *   its results out, so eager calls from several threads or streams may share
+ *   one workspace.  A captured call is not ordered against other calls: its
+ *   replays need a workspace of their own, or ordering by the caller.  Argument errors
  *   return FA_ERR_INVALID_ARG before anything is queued; dtype, d and mask as
  *   for fa_forward_masked.
  */

@@ -326,6 +326,7 @@ struct HostPipe {
   cudaEvent_t in_done[2] = {nullptr, nullptr};   // chunk's q, k, v are on the device
   cudaEvent_t fwd_done[2] = {nullptr, nullptr};  // chunk's forward has finished
   cudaEvent_t out_done[2] = {nullptr, nullptr};  // chunk's o, lse are back on the host
+  bool last_eager = false;                       // out_done last recorded outside a graph capture
 };
 HostPipe g_pipes[64];
 
@@ -449,6 +450,18 @@ fa_status fa_forward_host(const void* q, const void* k, const void* v, void* o, 
   FA_HOST_CUDA(cudaEventRecord(hp.start, s), "fa_forward_host: event record");
   FA_HOST_CUDA(cudaStreamWaitEvent(hp.h2d, hp.start, 0), "fa_forward_host: stream wait");
   FA_HOST_CUDA(cudaStreamWaitEvent(hp.d2h, hp.start, 0), "fa_forward_host: stream wait");
+  // The previous call on this device (perhaps from another thread, on another
+  // stream, with the same workspace) must have copied its results out before
+  // this call's first copy in: its last copy-out events cover all of its work.
+  // Only eager calls are ordered this way; a wait across a graph capture's edge
+  // is not allowed, and a captured call is ordered by whoever replays it.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  FA_HOST_CUDA(cudaStreamIsCapturing(s, &cap), "fa_forward_host: capture query");
+  const bool eager = cap == cudaStreamCaptureStatusNone;
+  if (eager && hp.last_eager)
+    for (int b = 0; b < 2; ++b)
+      FA_HOST_CUDA(cudaStreamWaitEvent(hp.h2d, hp.out_done[b], 0), "fa_forward_host: stream wait");
+  hp.last_eager = eager;
   for (int64_t c = 0; c < chunks; ++c) {
     const int b = static_cast<int>(c & 1);
     const int64_t h0 = c * hpc;

@@ -12,6 +12,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
+import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfa.so")
@@ -192,6 +193,7 @@ def forward(q, k, v, scale: float | None = None, out=None, lse=None, return_lse:
 
 
 _host_ws = {}
+_host_ws_lock = threading.Lock()
 
 
 def forward_host(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool = False,
@@ -227,13 +229,20 @@ def forward_host(q, k, v, scale: float | None = None, out=None, lse=None, causal
         need = int(lib().fa_forward_host_workspace_size(B, H, Nq, Nkv, d, code, int(heads_per_chunk)))
         if need == 0:
             raise FAError(FA_ERR_INVALID_ARG, "fa_forward_host_workspace_size rejected the arguments")
-        ws = _host_ws.get(dev.index)
-        if ws is None or ws.numel() < need:
-            ws = torch.empty(need, dtype=torch.uint8, device=dev)
-            _host_ws[dev.index] = ws
-        _check(lib().fa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d, code,
-                                     float(scale), FA_MASK_CAUSAL if causal else FA_MASK_NONE,
-                                     int(heads_per_chunk), _ptr(ws), ws.numel(), _stream_ptr(stream)))
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        # One cached workspace per device, shared by all threads and streams:
+        # the library orders the calls that use it, and record_stream keeps the
+        # caching allocator from handing it out again while a call on another
+        # stream may still read it after it has been replaced by a larger one.
+        with _host_ws_lock:
+            ws = _host_ws.get(dev.index)
+            if ws is None or ws.numel() < need:
+                ws = torch.empty(need, dtype=torch.uint8, device=dev)
+                _host_ws[dev.index] = ws
+            _check(lib().fa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nkv, d, code,
+                                         float(scale), FA_MASK_CAUSAL if causal else FA_MASK_NONE,
+                                         int(heads_per_chunk), _ptr(ws), ws.numel(), _stream_ptr(s)))
+            ws.record_stream(s)
     return out, lse
 
 

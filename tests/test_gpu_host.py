@@ -75,3 +75,40 @@ def test_host_forward_pageable_inputs_and_reuse():
     fa.device_status()
     for got, ref in ((a, r1), (b, r2)):
         assert torch.equal(got[0], ref[0].cpu()) and torch.equal(got[1], ref[1].cpu())
+
+
+def test_host_forward_from_two_threads():
+    """Two host threads call the host-buffer forward at once, each on its own
+    stream: the library serialises them on its per-device copy streams and
+    workspace bookkeeping, and both results are exact."""
+    import threading
+
+    import torch
+    B, H, N, d = 2, 4, 256, 128
+    data = [make_qkv(40 + t, B, H, N, N, d, "bf16")[1] for t in range(2)]
+    refs = [fa.forward(dv["q"], dv["k"], dv["v"]) for dv in data]
+    torch.cuda.synchronize()
+    results = [None, None]
+    errors = []
+
+    def run(t):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                hq, hk, hv = (_host(data[t][n]) for n in ("q", "k", "v"))
+                for _ in range(3):
+                    results[t] = fa.forward_host(hq, hk, hv, heads_per_chunk=3, stream=st)
+            st.synchronize()
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    fa.device_status()
+    for t in range(2):
+        assert torch.equal(results[t][0], refs[t][0].cpu()) and torch.equal(results[t][1], refs[t][1].cpu())
+
