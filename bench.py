@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
-    "fwd_prefill": {"src": "691ff72798141c79", "bytes": 402787072 + 121707008},
+    "fwd_prefill": {"src": "717c0a53fea59bca", "bytes": 402734592 + 119698944},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
     "bwd_train": {"src": "76efbd405334fe22", "bytes": 404883200 + 222745088},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is

@@ -56,6 +56,15 @@
 // bytes per k-step), P̃ is stored as E4M3 (lazy rescaling keeps it <= 256, inside
 // E4M3's ±448) and ℓ sums the unrounded fp32 values; O leaves as bf16.
 //
+// E4M3 hands P̃ over in two halves: a softmax warp whose rows keep their
+// reference max signals p_half once P̃ of the first 64 keys is in TMEM, and the
+// MMA warp issues that half of P̃_iV_j while the second half's exponentials are
+// still running (a warp that rescales O signals both halves after the rescale,
+// so no P̃V MMA reads O before it).  The MMAs and their order are unchanged, so
+// the results are identical.  Measured on GB300: E4M3 +6–9 %; the bf16
+// instances lost 3 % (d = 64) and 16 % (d = 128) with the same split, so they
+// hand over the whole tile at once.
+//
 // Lazy rescaling: a row keeps its reference max m until a tile's max exceeds
 // it by more than kRescaleLog2 (base-2 units).  Until then P̃ = 2^(σ'S − m) is
 // at most 2^kRescaleLog2 and O, ℓ keep accumulating against the same m, so the
@@ -102,6 +111,7 @@ struct FwdBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  uint64_t p_half[kQT];  // E4M3: P̃_i(j) of the first 64 keys in TMEM, O_i rescaled
 };
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernFwd << 8) | s; }
@@ -165,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     for (int i = 0; i < kQT; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_half[i], 128);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -246,13 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         const bool next = j + 1 < T;
         const uint32_t kb = sR + ((tv + 1) % L::kRing) * L::kSlot;
         for (int i = 0; i < kQT && ok; ++i) {
-          if (!(ok = W::wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
+          if (!(ok = W::wait(FP8 ? &bars->p_half[i] : &bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
           if (i == 0 && next && !(ok = ring_wait(tv + 1, 6))) break;
           tc_fence_after();
           // O_i += P̃_i V_j: A = P̃_i from S_i's TMEM columns (32 bytes of keys = 8
           // columns per k-step), B = V_j read MN-major (head dim contiguous).
+          constexpr int kHalf = kBN / L::kStepK / 2;
 #pragma unroll
           for (int kk = 0; kk < kBN / L::kStepK; ++kk) {
+            if (FP8 && kk == kHalf) {  // the second half of P̃_i
+              if (!(ok = W::wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
+              tc_fence_after();
+            }
             const uint64_t bd = sdesc_sw128(vb + kk * L::kStepK * 128, kTileBytes, 1024);
             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
             if (FP8)
@@ -260,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             else
               mma_bf16_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
           }
+          if (FP8 && !ok) break;
           if (next) issue_s(i, kb);
           mma_commit(&bars->s_full[i]);
         }
@@ -335,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       const bool need = m_cand > m_run + kRescaleLog2;  // always true while m_run = −∞
       const float m_new = need ? m_cand : m_run;
       const float corr = need ? ex2_approx(m_run - m_new) : 1.f;
+      const bool resc = j >= 1 && __any_sync(0xffffffffu, need);  // this warp rescales O
       float rs[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) rs[i] = 0.f;
@@ -367,12 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           tmem_st16(tmem + lane_base + s_col + 16 * hf, reinterpret_cast<uint32_t(&)[16]>(w));
         else
           tmem_st32(tmem + lane_base + s_col + 32 * hf, w);
+        if (FP8 && hf == 0 && !resc) {  // E4M3: the first half goes early
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->p_half[qt]);
+        }
       }
       const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       l_run = l_run * corr + rsum;
       // O_i is stable here (its last update came before S_i(j)); rescale it in
       // TMEM only when some row of this warp moved its reference max.
-      if (j >= 1 && __any_sync(0xffffffffu, need)) {
+      if (FP8 ? resc : (j >= 1 && __any_sync(0xffffffffu, need))) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -387,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       }
       tmem_wait_st();
       tc_fence_before();
+      if (FP8 && resc) mbar_arrive(&bars->p_half[qt]);
       mbar_arrive(&bars->p_full[qt]);
       m_run = m_new;
     }
