@@ -127,6 +127,29 @@ fa_status make_map(CUtensorMap* tm, const void* base, int B, int H, int N, int d
   return FA_OK;
 }
 
+// 5-D bf16 map over a paged cache [num_blocks, H_kv, bs, 128] that loads one
+// page of one head as a single box laid out for the tensor cores: dimensions
+// (64 columns, 8 rows, 2 column halves, bs/8 row groups, page·H_kv + head), so
+// a page lands as [row group][half][8 rows][128 bytes] and every 8-row group of
+// a key tile is 2 KB from the next whatever the page size.  The column halves
+// (stride 128 bytes) come after the rows (stride 256 bytes); page and head
+// merge into one dimension because a page's heads are contiguous.
+fa_status make_page_map5(CUtensorMap* tm, const void* base, int num_blocks, int H_kv, int bs, const char* name) {
+  EncodeTiledFn enc;
+  fa_status s = get_encoder(&enc);
+  if (s != FA_OK) return s;
+  cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(bs / 8),
+                        static_cast<cuuint64_t>(num_blocks) * static_cast<cuuint64_t>(H_kv)};
+  cuuint64_t strides[4] = {256, 128, 8 * 256, static_cast<cuuint64_t>(bs) * 256};
+  cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(bs / 8), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return FA_OK;
+}
+
 bool bad_scale(float scale) { return !(std::isfinite(scale) && scale > 0.f); }
 
 fa_status check_launch(const char* what, int n) {
@@ -754,14 +777,18 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
   memset(&t, 0, sizeof(t));
   const int64_t qspan = static_cast<int64_t>(B) * H_q * d;
   if ((r = make_map(&t.tm_q, q, 1, 1, B * H_q, d, qspan, qspan, d, "q")) != FA_OK) return r;
-  // Pages as a 4-D tensor {d, block_size, H_kv, num_blocks}; one box is one page of one head.
-  const int64_t page = static_cast<int64_t>(block_size) * d;
-  if ((r = make_map(&t.tm_k, k_cache, num_blocks, H_kv, block_size, d, H_kv * page, page, d, "k_cache",
-                    block_size)) != FA_OK)
-    return r;
-  if ((r = make_map(&t.tm_v, v_cache, num_blocks, H_kv, block_size, d, H_kv * page, page, d, "v_cache",
-                    block_size)) != FA_OK)
-    return r;
+  if (d == 128) {  // one box per page of one head, both 64-column halves
+    if ((r = make_page_map5(&t.tm_k, k_cache, num_blocks, H_kv, block_size, "k_cache")) != FA_OK) return r;
+    if ((r = make_page_map5(&t.tm_v, v_cache, num_blocks, H_kv, block_size, "v_cache")) != FA_OK) return r;
+  } else {  // d = 64: pages as a 4-D tensor {d, block_size, H_kv, num_blocks}
+    const int64_t page = static_cast<int64_t>(block_size) * d;
+    if ((r = make_map(&t.tm_k, k_cache, num_blocks, H_kv, block_size, d, H_kv * page, page, d, "k_cache",
+                      block_size)) != FA_OK)
+      return r;
+    if ((r = make_map(&t.tm_v, v_cache, num_blocks, H_kv, block_size, d, H_kv * page, page, d, "v_cache",
+                      block_size)) != FA_OK)
+      return r;
+  }
   t.block_table = block_table;
   t.seq_lens = seq_lens;
   t.max_blocks = max_blocks;

@@ -32,8 +32,12 @@
 // split's last, partial tile the softmax warp zeroes the V rows past the end
 // (slots of a partly filled page hold stale data) before P̃V runs.
 // The boxes of one tile are issued by different lanes of the producer warp at
-// once; small pages (2 KB boxes at 16 keys) need that to keep enough copies in
-// flight.
+// once; small pages need that to keep enough copies in flight.  At d = 128 a
+// page of one head is a single box of a 5-D view (64 columns, 8 rows, 2 column
+// halves, bs/8 row groups, page·H_kv + head) that lands as [row group][half]
+// [8 rows][128 bytes]: the tile's 8-row groups are 2 KB apart and its column
+// halves 1 KB apart for any page size, and one box per page (4 KB at 16 keys)
+// replaces two half-width boxes.  The MMA descriptors follow that layout.
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -55,6 +59,10 @@ constexpr int kMaxRing = 10;
 template <int D>
 struct TcCfg {
   static constexpr int kNKB = D / 64;
+  // Paged d = 128 tiles use the grouped layout above: byte offsets of the next
+  // 8-row group and of the second column half.
+  static constexpr int kPgGroup = 2048;
+  static constexpr int kPgHalf = 1024;
   static constexpr int kSlot = kNKB * kTileBytes;
   static constexpr int kRing = D == 64 ? 10 : 5;
   static constexpr int kOffQ = 0;
@@ -84,6 +92,7 @@ template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid_constant__ DecodeTcParams p) {
   using C = TcCfg<D>;
   constexpr int kSlot = C::kSlot, kRing = C::kRing, kOffQ = C::kOffQ, kOffR = C::kOffR;
+  constexpr bool kPg5 = PAGED && D == 128;  // K/V tiles in the grouped page layout
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -203,9 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
               blk = page_id(t0);
             else
               row = bs;  // wholly out of range: zero fill
-            for (int kb = 0; kb < C::kNKB; ++kb)
-              tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes + lane * bs * 128, tm,
-                          &bars->r_full[slot], kb * 64, row, hkv, blk);
+            if constexpr (D == 128) {
+              tma_load_5d(smem + kOffR + slot * kSlot + lane * bs * 256, tm, &bars->r_full[slot], 0, 0, 0,
+                          row >> 3, blk * p.Hkv + hkv);
+            } else {
+              for (int kb = 0; kb < C::kNKB; ++kb)
+                tma_load_4d(smem + kOffR + slot * kSlot + kb * kTileBytes + lane * bs * 128, tm,
+                            &bars->r_full[slot], kb * 64, row, hkv, blk);
+            }
           }
         }
         ++issued;
@@ -231,9 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         tc_fence_after();
         const uint32_t vb = sR + slot * kSlot;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)  // A = P̃(jj) from its S buffer's TMEM columns
-          mma_bf16_ts(tmem + kColO, tmem + (jj & 1) * kBN + kk * 8, sdesc_sw128(vb + kk * 2048, kTileBytes, 1024),
-                      kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk) {  // A = P̃(jj) from its S buffer's TMEM columns
+          // 16 keys per k-step: two 8-key groups; the head dim's 64-column halves are the MN blocks.
+          const uint64_t bd = kPg5 ? sdesc_sw128(vb + kk * 2 * C::kPgGroup, C::kPgHalf, C::kPgGroup)
+                                   : sdesc_sw128(vb + kk * 2048, kTileBytes, 1024);
+          mma_bf16_ts(tmem + kColO, tmem + (jj & 1) * kBN + kk * 8, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit(&bars->p_free);
         mma_commit(&bars->r_empty[slot]);
         return true;
@@ -251,8 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + sb * kBN, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdescS,
-                      kk > 0 ? 1u : 0u);
+          const uint64_t bd = kPg5 ? sdesc_sw128(kb + (kk >> 2) * C::kPgHalf + (kk & 3) * 32, 16, C::kPgGroup)
+                                   : sdesc_sw128(kb + off, 16, 1024);
+          mma_bf16_ss(tmem + sb * kBN, sdesc_sw128(sQ + off, 16, 1024), bd, kIdescS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full[sb]);
         mma_commit(&bars->r_empty[slot]);
@@ -368,10 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gqa_tc_kernel(const __grid
         uint8_t* vt = smem + kOffR + (t % kRing) * kSlot;
         for (int rr = max(valid, 0) + lane; rr < kBN; rr += 32)
 #pragma unroll
-          for (int kb = 0; kb < C::kNKB; ++kb)
+          for (int kb = 0; kb < C::kNKB; ++kb) {
+            // Byte offset of key row rr's 128 bytes in column half kb.
+            const int ro = kPg5 ? (rr >> 3) * C::kPgGroup + kb * C::kPgHalf + (rr & 7) * 128 : kb * kTileBytes + rr * 128;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(vt + kb * kTileBytes + rr * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vt + ro + q * 16) = make_uint4(0, 0, 0, 0);
+          }
       }
       fence_proxy_async_smem();
       tc_fence_before();
