@@ -203,7 +203,10 @@ def forward_host(q, k, v, scale: float | None = None, out=None, lse=None, causal
     library streams (b, h) chunks through a device workspace, overlapping the
     copies in and out with the forward.  Returns (O, LSE) as CPU tensors
     (page-locked when allocated here); they are valid once ``stream`` (default:
-    the device's current stream) has been synchronised."""
+    the device's current stream) has been synchronised.  The workspace is cached
+    per device and shared: eager calls from several threads or streams are
+    ordered by the library, while a call captured in a CUDA graph is not, so
+    replays must not overlap other calls on that device."""
     torch = _torch()
     for t in (q, k, v):
         if t.is_cuda or not t.is_contiguous():
