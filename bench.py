@@ -44,12 +44,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
-    "fwd_prefill": {"src": "717c0a53fea59bca", "bytes": 402734592 + 119698944},
+    "fwd_prefill": {"src": "469cb9fe0d1a4bab", "bytes": 402715392 + 121430016},
     # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
-    "bwd_train": {"src": "76efbd405334fe22", "bytes": 404883200 + 222745088},
+    "bwd_train": {"src": "517a4454ffb25174", "bytes": 404839168 + 223034368},
     # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
     # proportional to B, stored here scaled to the B=64 launch
-    "decode_split": {"src": "01d15147b0d37913", "bytes": (1073837056 + 6951168) * 8},
+    "decode_split": {"src": "71b693dc62ea91ee", "bytes": (1073836800 + 7016960) * 8},
 }
 
 
