@@ -96,6 +96,42 @@ def test_fp8_forward_causal():
     _check(53, 1, 2, 384, 384, causal=True)
 
 
+def test_fp8_forward_rising_scores_rescale_mid_sequence():
+    """Key magnitudes ramp from 1x to 5x along the sequence, so a row's max
+    score keeps rising and moves past its reference max by more than 2^8
+    (base 2) in a later key tile.  Such a warp rescales O and hands both halves
+    of P̃ to the MMA warp after the rescale instead of the first half early.
+    The test first checks, on the CPU, that the data does trigger that rescale,
+    then holds the kernel to the same derived bound as the other cases."""
+    import torch
+    B, H, Nq, Nkv, d = 1, 2, 256, 1024, 128
+    qc, qf = _quant(56, "q", B, H, Nq, d, 1.0)
+    vc, vf = _quant(56, "v", B, H, Nkv, d, 1.0)
+    ramp = np.linspace(1.0, 5.0, Nkv, dtype=np.float32)
+    kx = inputs.normal_tensor(56, "k", B, H, Nkv, d, "fp32") * ramp[None, None, :, None]
+    kc = inputs.f32_to_e4m3_bits(kx)
+    kf = inputs.e4m3_bits_to_f32(kc).astype(np.float64)
+    scale = 1 / math.sqrt(d)
+    # Reference-max bookkeeping of the kernel (base 2, threshold 2^8), per row and key tile.
+    s2 = scale * math.log2(math.e) * np.einsum("bhqd,bhkd->bhqk", qf, kf)
+    tile_max = s2.reshape(B, H, Nq, Nkv // 128, 128).max(axis=-1)
+    m_ref = tile_max[..., 0]
+    rescales = 0
+    for j in range(1, Nkv // 128):
+        moved = tile_max[..., j] > m_ref + 8.0
+        rescales += int(moved.sum())
+        m_ref = np.where(moved, tile_max[..., j], m_ref)
+    assert rescales >= Nq, rescales  # most rows rescale at least once after the first tile
+    o, lse = fa.forward_fp8(*(torch.from_numpy(c).cuda() for c in (qc, kc, vc)), scale=scale)
+    fa.device_status()
+    for h in range(H):
+        ro, rl = oracle.attention_forward(qf[0, h], kf[0, h], vf[0, h], scale)
+        bnd = _bound(qf[0, h], kf[0, h], vf[0, h], scale, False)
+        got = cpu64(o[0, h])
+        assert np.all(np.abs(got - ro) <= bnd), (h, float(np.max(np.abs(got - ro) - bnd)))
+        assert np.max(np.abs(cpu64(lse[0, h]) - rl)) <= 1e-3 * max(1.0, float(np.abs(rl).max()) / 8), h
+
+
 def test_fp8_relative_error_matches_the_rounding_rms_on_spread_attention():
     """With N(0,1) inputs attention is spread over many keys, so O's relative
     error follows the RMS relative error of rounding P̃ to E4M3: for a 3-bit
