@@ -101,6 +101,40 @@ def test_forward_bf16_large_scores():
     assert max_abs(cpu64(lse), ref_lse) <= TOL_LSE_BF16 * max(1.0, float(np.abs(ref_lse).max()) / 8)
 
 
+@pytest.mark.parametrize("d,causal", [(128, False), (64, False), (128, True)])
+def test_forward_bf16_rising_scores_rescale_mid_sequence(d, causal):
+    """Key magnitudes ramp from 1x to 5x along the sequence, so rows move their
+    reference max (by more than 2^8 in base 2) in later key tiles and O is
+    rescaled in TMEM mid-sequence.  A CPU check first confirms that the data
+    triggers such rescales; the bound is the one derived for large scores."""
+    import torch
+    B, H, N = 1, 2, 1024
+    host, dev = make_qkv(6, B, H, N, N, d, "bf16")
+    ramp = torch.linspace(1.0, 5.0, N, device="cuda").view(1, 1, N, 1)
+    k = (dev["k"].float() * ramp).to(torch.bfloat16)
+    k64 = cpu64(k)
+    q64 = f64(host["q"], "bf16")
+    scale = 1 / math.sqrt(d)
+    s2 = scale * math.log2(math.e) * np.einsum("bhqd,bhkd->bhqk", q64, k64)
+    if causal:
+        s2 = np.where(oracle.causal_visible(np.arange(N), N, N)[None, None], s2, -np.inf)
+    tile_max = s2.reshape(B, H, N, N // 128, 128).max(axis=-1)
+    m_ref = tile_max[..., 0]
+    rescales = 0
+    for j in range(1, N // 128):
+        moved = tile_max[..., j] > m_ref + 8.0
+        rescales += int(moved.sum())
+        m_ref = np.where(moved, tile_max[..., j], m_ref)
+    assert rescales >= N // 2, rescales
+    o, lse = fa.forward(dev["q"], k, dev["v"], causal=causal)
+    fa.device_status()
+    v64 = f64(host["v"], "bf16")
+    for h in range(H):
+        ref_o, ref_lse = oracle.attention_rows(q64[0, h], k64[0, h], v64[0, h], scale, np.arange(N), causal=causal)
+        assert max_abs(cpu64(o[0, h]), ref_o) <= 2.0 ** -7 * float(np.abs(v64).max()) + 1e-3, h
+        assert max_abs(cpu64(lse[0, h]), ref_lse) <= TOL_LSE_BF16 * max(1.0, float(np.abs(ref_lse).max()) / 8), h
+
+
 def test_forward_strided_inputs():
     """Q/K/V/O as [B, N, H, d] buffers viewed as [B, H, N, d]."""
     import torch
