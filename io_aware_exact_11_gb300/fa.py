@@ -316,7 +316,7 @@ def decode_splitkv(q, k, v, n_splits: int | None = None, scale: float | None = N
 
 def decode_splitkv_gqa(q, k, v, n_splits: int | None = None, scale: float | None = None, out=None, lse=None,
                        workspace=None, stream=None):
-    """Grouped-query split-KV decode: q [B,Hq,1,d], k/v [B,Hkv,Nkv,d], Hq = G·Hkv (G <= 32).
+    """Grouped-query split-KV decode: q [B,Hq,1,d], k/v [B,Hkv,Nkv,d], Hq = G·Hkv (G <= 128).
     n_splits=None takes the library's choice for the shape."""
     torch = _torch()
     _check_cuda(q, k, v)
