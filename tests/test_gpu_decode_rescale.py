@@ -1,13 +1,14 @@
 """Decode with a rising running max: splits rescale mid-range.
 
 Key magnitudes ramp from 1x to 9x along the sequence, so within each of two
-splits a query row's tile maxima (nearly always) climb by more than 2^8
-(base 2) and the kernels rescale their partial (m, ℓ, o) on the way: the single-head CUDA-core
-split kernel, the grouped tensor-core kernel, and both over a paged cache (the
-grouped one in its one-box-per-page layout).  A CPU check first confirms the
-rise in at least three of four (row, split) pairs; results are then held to
-the large-score bound (bf16 P̃ and bf16 O each round with relative error <= 2^-8, so O is within
-2^-7·max|V| plus fp32 noise) and LSE to 1e-3 scaled by its magnitude.
+splits a query row's tile maxima (nearly always) climb by more than 2^8 in
+base 2, and the kernels rescale their partial (m, ℓ, o) on the way: the
+single-head CUDA-core split kernel, the grouped tensor-core kernel, and both
+over a paged cache (the grouped one in its one-box-per-page layout).  A CPU
+check first confirms the rise in at least three of four (row, split) pairs.
+Results are then held to the large-score bound: bf16 P̃ and bf16 O each round
+with relative error <= 2^-8, so O is within 2^-7·max|V| plus fp32 noise; LSE
+is within 1e-3 scaled by its magnitude.
 """
 
 import math
