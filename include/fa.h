@@ -221,7 +221,8 @@ FA_API fa_status fa_decode_splitkv_gqa(const void* q, const void* k, const void*
  *   FA_ERR_INVALID_ARG.  Cache slots past a sequence's end may hold anything.
  *   q [B,H_q,1,d]; o [B,H_q,1,d]; lse [B,H_q] (or NULL); workspace as for
  *   fa_decode_splitkv with H = H_q.
- *   Supported: FA_BF16, d = 64 or 128, block_size ∈ {16, 32, 64, 128}, H_q = G·H_kv, G ≤ 128.
+ *   Supported: FA_BF16, d = 64 or 128, block_size ∈ {16, 32, 64, 128}, H_q = G·H_kv, G ≤ 128,
+ *   num_blocks·H_kv ≤ 2^31 − 1 (FA_ERR_UNSUPPORTED otherwise).
  */
 FA_API fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                                  const int32_t* seq_lens, void* o, float* lse, int B, int H_q, int H_kv,

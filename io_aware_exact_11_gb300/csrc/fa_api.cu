@@ -5,6 +5,7 @@
 // events fa_forward_host pipelines its transfers with.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -733,6 +734,9 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
   if (B > 65535 || H_q > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: B and H must be <= 65535");
   if (static_cast<int64_t>(max_blocks) * block_size > (1 << 30))
     return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: max_blocks * block_size too large");
+  // The grouped kernel addresses a page of one head as page·H_kv + head in a 32-bit TMA coordinate.
+  if (static_cast<int64_t>(num_blocks) * H_kv > INT32_MAX)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: num_blocks * H_kv too large");
   if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: scale must be finite and > 0");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
