@@ -152,8 +152,8 @@ def test_gqa_decode_validates_before_cuda(L):
 
 
 def test_paged_decode_validates_before_cuda(L):
-    def dec(bs=16, Hq=28, Hkv=4, d=128, wsb=1 << 24, table=FAKE):
-        return L.fa_decode_paged(FAKE, FAKE, FAKE, table, FAKE, FAKE, None, 2, Hq, Hkv, 100, bs, 64, d, fa.FA_BF16,
+    def dec(bs=16, Hq=28, Hkv=4, d=128, wsb=1 << 24, table=FAKE, nb=100):
+        return L.fa_decode_paged(FAKE, FAKE, FAKE, table, FAKE, FAKE, None, 2, Hq, Hkv, nb, bs, 64, d, fa.FA_BF16,
                                  0.1, 8, FAKE, wsb, None)
     assert dec(bs=24) == fa.FA_ERR_UNSUPPORTED
     assert dec(bs=256) == fa.FA_ERR_UNSUPPORTED
@@ -162,6 +162,8 @@ def test_paged_decode_validates_before_cuda(L):
     assert dec(table=None) == fa.FA_ERR_INVALID_ARG
     assert dec(wsb=16) == fa.FA_ERR_INVALID_ARG
     assert dec(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert dec(nb=1 << 30) == fa.FA_ERR_UNSUPPORTED              # page·H_kv + head past a 32-bit coordinate
+    assert b"num_blocks" in L.fa_get_last_error()
 
 
 def test_host_forward_workspace_size(L):
