@@ -440,6 +440,19 @@ def run_ours(args, ws, rank, local):
                                                  "peak_source": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)"}}
         del q8, k8, v8, of, lf
 
+    if "d64" in extras:
+        # ---------------- head dim 64 at the prefill shape (the other head dim the kernels are built for)
+        B6, H6, N6, d6 = PREFILL["B"], PREFILL["H"], PREFILL["N"], 64
+        q6, k6, v6 = (randn((B6, H6, N6, d6), s) for s in (31, 32, 33))
+        o6 = torch.empty_like(q6)
+        l6 = torch.empty((B6, H6, N6), dtype=torch.float32, device=dev)
+        n_6 = max(5, min(args.steps, 50))
+        t_6 = timed(lambda: fa.forward(q6, k6, v6, out=o6, lse=l6), n_6, 2) / n_6
+        f6 = fwd_flops(B6, H6, N6, d6)
+        extra["d64_prefill_fwd"] = {"workload": "B=4 H=32 N=4096 d=64 bf16", "tflops": f6 / t_6 / 1e12,
+                                    "ms": t_6 * 1e3, "frac_of_bf16_peak": f6 / t_6 / 1e12 / peak}
+        del q6, k6, v6, o6, l6
+
     if "causal" in extras:
         # ---------------- causal mask: prefill forward and training backward
         Bc, Hc, Nc = PREFILL["B"], PREFILL["H"], PREFILL["N"]
@@ -507,7 +520,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
-    ap.add_argument("--extras", default="long,decode,gqa,paged,train,causal,fp8",
+    ap.add_argument("--extras", default="long,decode,gqa,paged,train,causal,fp8,d64",
                     help="comma list of extra workloads measured after the headline")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="decode batch B (64 is the configured workload; smaller only for profiling)")
