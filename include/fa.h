@@ -27,7 +27,7 @@
  *   - Errors.  FA_ERR_INVALID_ARG: null pointer, non-positive size, bad
  *     stride, misaligned pointer (16-byte alignment is required), scale not
  *     finite and > 0, workspace too small.  FA_ERR_UNSUPPORTED: a head dim,
- *     dtype or size this build has no kernel for; there is never a silent
+ *     dtype or size the library has no kernel for; there is never a silent
  *     fallback to another algorithm.  FA_ERR_CUDA: a launch or earlier
  *     asynchronous CUDA error.  FA_ERR_DEVICE_TIMEOUT: a kernel gave up on a
  *     pipeline wait (reported by fa_device_status).  On any error the
