@@ -43,12 +43,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum), keyed by the sha256 of the kernel's sources at capture
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # profiles/fwd_kernel_prefill_B4_H32_N4096_d128.md
+    # the forward kernel at the prefill shape (B=4 H=32 N=4096 d=128), one launch
     "fwd_prefill": {"src": "469cb9fe0d1a4bab", "bytes": 402715392 + 121430016},
-    # profiles/bwd_main_kernel_train_B2_H16_N8192_d128.md (bwd_main_kernel only)
+    # the backward's main kernel at the training shape (B=2 H=16 N=8192 d=128), one launch
     "bwd_train": {"src": "517a4454ffb25174", "bytes": 404839168 + 223034368},
-    # profiles/decode_split_kernel_B8_H32_Nkv8192_d128.md: captured at B=8, traffic is
-    # proportional to B, stored here scaled to the B=64 launch
+    # the split decode kernel, captured at B=8 (H=32 N_kv=8192 d=128); its traffic is
+    # proportional to B, so it is stored here scaled to the B=64 launch
     "decode_split": {"src": "71b693dc62ea91ee", "bytes": (1073836800 + 7016960) * 8},
 }
 
@@ -168,6 +168,54 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+class SmClockPoller:
+    """Reads the SM clock (MHz) through NVML while a timed region runs.
+
+    Reading only: nothing here changes a GPU setting.  If NVML is not
+    available the poller returns no samples."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self._ct = ctypes
+        self.nv = None
+        self.h = ctypes.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0 or nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                return
+            self.nv = nv
+        except Exception:
+            self.nv = None
+
+    def read(self):
+        if self.nv is None:
+            return None
+        v = self._ct.c_uint()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, self._ct.byref(v)) != 0:
+            return None
+        return float(v.value)
+
+    def poll_until(self, event, samples):
+        """Sample until `event` (a recorded torch.cuda.Event) has completed."""
+        while not event.query():
+            x = self.read()
+            if x is not None:
+                samples.append(x)
+            time.sleep(0.0005)
+
+
+def median(xs):
+    if not xs:
+        return None
+    s = sorted(xs)
+    return s[len(s) // 2]
+
+
 # --------------------------------------------------------------- CPU oracle
 _HEAD = {}
 
@@ -249,12 +297,26 @@ def run_ours(args, ws, rank, local):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev)
+    poller = SmClockPoller(local)
+    clock_log = {}  # workload -> SM MHz samples taken during its timed region
+    peak_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+
+    def per_clock(tflops, key, peak_tf):
+        """The workload's median SM clock, its TFLOP/s per GHz, and its fraction of
+        the peak with both taken per GHz (the peak at the clock it was measured at)."""
+        mhz = median(clock_log.get(key, []))
+        out = {"sm_mhz_median": mhz, "sm_samples": len(clock_log.get(key, []))}
+        if mhz:
+            out["tflops_per_ghz"] = tflops / (mhz / 1e3)
+            if peak_mhz:
+                out["frac_of_peak_per_clock"] = (tflops / mhz) / (peak_tf / float(peak_mhz))
+        return out
 
     def randn(shape, seed):
         gen.manual_seed(seed * 1000003 + rank)
         return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
 
-    def timed(fn, steps, warmup):
+    def timed(fn, steps, warmup, key=None):
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
@@ -265,6 +327,8 @@ def run_ours(args, ws, rank, local):
         for _ in range(steps):
             fn()
         e1.record(stream)
+        if key is not None:
+            poller.poll_until(e1, clock_log.setdefault(key, []))
         torch.cuda.synchronize()
         barrier(ws)
         return e0.elapsed_time(e1) / 1e3
@@ -284,7 +348,7 @@ def run_ours(args, ws, rank, local):
     fa.device_status()
     launches0 = fa.launch_count()
     with ClockSampler(local) as clk:
-        el = timed(step, args.steps, 0)
+        el = timed(step, args.steps, 0, key="prefill")
     launches = fa.launch_count() - launches0
     fa.device_status()
     el_max = max_over_ranks(el, ws, dev)
@@ -321,10 +385,11 @@ def run_ours(args, ws, rank, local):
         ol = torch.empty_like(ql)
         ll = torch.empty((Bl, Hl, Nl), dtype=torch.float32, device=dev)
         n_long = max(2, min(args.steps // 10, 10))
-        t_long = timed(lambda: fa.forward(ql, kl, vl, out=ol, lse=ll), n_long, 1) / n_long
+        t_long = timed(lambda: fa.forward(ql, kl, vl, out=ol, lse=ll), n_long, 1, key="long") / n_long
         fl = fwd_flops(Bl, Hl, Nl, d)
         extra["long_forward"] = {"workload": "B=1 H=32 N=32768 d=128 bf16", "tflops": fl / t_long / 1e12,
-                                 "ms": t_long * 1e3, "frac_of_bf16_peak": fl / t_long / 1e12 / peak}
+                                 "ms": t_long * 1e3, "frac_of_bf16_peak": fl / t_long / 1e12 / peak,
+                                 **per_clock(fl / t_long / 1e12, "long", peak)}
         del ql, kl, vl, ol, ll
 
     if "decode" in extras:
@@ -337,13 +402,13 @@ def run_ours(args, ws, rank, local):
         ws_d = torch.empty(fa.decode_workspace_size(Bd, Hd, d, S), dtype=torch.uint8, device=dev)
         n_dec = max(5, min(args.steps, 50))
         t_dec = timed(lambda: fa.decode_splitkv(qd, kd, vd, n_splits=S, out=od, lse=ld, workspace=ws_d),
-                      n_dec, 2) / n_dec
+                      n_dec, 2, key="decode") / n_dec
         kv_bytes = 2.0 * Bd * Hd * Nd * d * 2
         dec_traffic = traffic_for("decode_split", ("fa_decode.cu", "sm103.cuh"))
         extra["decode"] = {"workload": f"B={Bd} H=32 S_q=1 N_kv=8192 d=128 bf16, 32 splits",
                            "hbm_gbs": kv_bytes / t_dec / 1e9, "tokens_per_s": Bd / t_dec, "ms": t_dec * 1e3,
                            "frac_of_hbm_peak": kv_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"]),
-                           "bytes_per_step": kv_bytes,
+                           "bytes_per_step": kv_bytes, "sm_mhz_median": median(clock_log.get("decode", [])),
                            "roofline": {"bound": "hbm", "achieved": kv_bytes / t_dec / 1e9,
                                         "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                                         "frac": kv_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"]),
@@ -370,11 +435,12 @@ def run_ours(args, ws, rank, local):
         n_g = max(5, min(args.steps, 50))
         # K/V (1.07 GB at B=64) is larger than L2, so back-to-back steps stream it from HBM.
         t_g = timed(lambda: fa.decode_splitkv_gqa(qg, kg, vg, n_splits=S, out=og, lse=lg, workspace=ws_g),
-                    n_g, 2) / n_g
+                    n_g, 2, key="gqa") / n_g
         kvb = 2.0 * Bg * Hkv * Ng * d * 2
         extra["gqa_decode"] = {"workload": f"B={Bg} Hq=28 Hkv=4 S_q=1 N_kv=8192 d=128 bf16, 4 splits",
                                "hbm_gbs": kvb / t_g / 1e9, "tokens_per_s": Bg / t_g, "ms": t_g * 1e3,
-                               "frac_of_hbm_peak": kvb / t_g / 1e9 / float(peaks["hbm_gbs"])}
+                               "frac_of_hbm_peak": kvb / t_g / 1e9 / float(peaks["hbm_gbs"]),
+                               "sm_mhz_median": median(clock_log.get("gqa", []))}
         del qg, kg, vg, og, lg, ws_g
 
     if "paged" in extras:
@@ -392,13 +458,15 @@ def run_ours(args, ws, rank, local):
             lp = torch.empty((Bp, Hq), dtype=torch.float32, device=dev)
             ws_p = torch.empty(fa.decode_workspace_size(Bp, Hq, d, S), dtype=torch.uint8, device=dev)
             n_p = max(5, min(args.steps, 50))
+            pkey = f"paged_{Hq}_{Hkv}_{bs}"
             t_p = timed(lambda: fa.decode_paged(qp, kp, vp, table, lens, n_splits=S, out=op, lse=lp, workspace=ws_p),
-                        n_p, 2) / n_p
+                        n_p, 2, key=pkey) / n_p
             kvb = 2.0 * Bp * Hkv * Np * d * 2
             extra[f"paged_decode_{Hq}q{Hkv}kv_page{bs}"] = {
                 "workload": f"B={Bp} Hq={Hq} Hkv={Hkv} N_kv=8192 d=128 bf16, {bs}-key pages, {S} splits",
                 "hbm_gbs": kvb / t_p / 1e9, "tokens_per_s": Bp / t_p, "ms": t_p * 1e3,
-                "frac_of_hbm_peak": kvb / t_p / 1e9 / float(peaks["hbm_gbs"])}
+                "frac_of_hbm_peak": kvb / t_p / 1e9 / float(peaks["hbm_gbs"]),
+                "sm_mhz_median": median(clock_log.get(pkey, []))}
             del qp, kp, vp, table, lens, op, lp, ws_p
 
     if "train" in extras:
@@ -410,14 +478,16 @@ def run_ours(args, ws, rank, local):
         dq, dk, dv = torch.empty_like(qt), torch.empty_like(kt), torch.empty_like(vt)
         ws_b = torch.empty(fa.backward_workspace_size(Bt, Ht, Nt, d), dtype=torch.uint8, device=dev)
         n_tr = max(3, min(args.steps // 5, 20))
-        t_f = timed(lambda: fa.forward(qt, kt, vt, out=ot, lse=lt), n_tr, 1) / n_tr
+        t_f = timed(lambda: fa.forward(qt, kt, vt, out=ot, lse=lt), n_tr, 1, key="train_fwd") / n_tr
         t_b = timed(lambda: fa.backward(qt, kt, vt, ot, lt, dot, dq=dq, dk=dk, dv=dv, workspace=ws_b),
-                    n_tr, 1) / n_tr
+                    n_tr, 1, key="train_bwd") / n_tr
         ff = fwd_flops(Bt, Ht, Nt, d)
         extra["train"] = {"workload": "B=2 H=16 N=8192 d=128 bf16", "fwd_tflops": ff / t_f / 1e12,
                           "bwd_tflops": 2.5 * ff / t_b / 1e12, "fwd_ms": t_f * 1e3, "bwd_ms": t_b * 1e3,
                           "fwd_frac_of_bf16_peak": ff / t_f / 1e12 / peak,
                           "bwd_frac_of_bf16_peak": 2.5 * ff / t_b / 1e12 / peak,
+                          "fwd_clock": per_clock(ff / t_f / 1e12, "train_fwd", peak),
+                          "bwd_clock": per_clock(2.5 * ff / t_b / 1e12, "train_bwd", peak),
                           "bwd_roofline": {"bound": "tensor", "achieved": 2.5 * ff / t_b / 1e12, "peak": peak,
                                            "unit": "TFLOP/s", "frac": 2.5 * ff / t_b / 1e12 / peak,
                                            "kernel": "time: whole backward (3 kernels); traffic: bwd_main_kernel",
@@ -430,11 +500,12 @@ def run_ours(args, ws, rank, local):
         of = torch.empty((Bf, Hf, Nf, d), dtype=torch.bfloat16, device=dev)
         lf = torch.empty((Bf, Hf, Nf), dtype=torch.float32, device=dev)
         n_f = max(5, min(args.steps, 50))
-        t_f8 = timed(lambda: fa.forward_fp8(q8, k8, v8, out=of, lse=lf), n_f, 2) / n_f
+        t_f8 = timed(lambda: fa.forward_fp8(q8, k8, v8, out=of, lse=lf), n_f, 2, key="fp8") / n_f
         ff8 = fwd_flops(Bf, Hf, Nf, d)
         peak8 = 2.0 * peak
         extra["fp8_prefill_fwd"] = {"workload": "B=4 H=32 N=4096 d=128 E4M3 in, bf16 out",
                                     "tflops": ff8 / t_f8 / 1e12, "ms": t_f8 * 1e3,
+                                    **per_clock(ff8 / t_f8 / 1e12, "fp8", peak8),
                                     "roofline": {"bound": "tensor", "achieved": ff8 / t_f8 / 1e12, "peak": peak8,
                                                  "unit": "TFLOP/s", "frac": ff8 / t_f8 / 1e12 / peak8,
                                                  "peak_source": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)"}}
@@ -447,10 +518,11 @@ def run_ours(args, ws, rank, local):
         o6 = torch.empty_like(q6)
         l6 = torch.empty((B6, H6, N6), dtype=torch.float32, device=dev)
         n_6 = max(5, min(args.steps, 50))
-        t_6 = timed(lambda: fa.forward(q6, k6, v6, out=o6, lse=l6), n_6, 2) / n_6
+        t_6 = timed(lambda: fa.forward(q6, k6, v6, out=o6, lse=l6), n_6, 2, key="d64") / n_6
         f6 = fwd_flops(B6, H6, N6, d6)
         extra["d64_prefill_fwd"] = {"workload": "B=4 H=32 N=4096 d=64 bf16", "tflops": f6 / t_6 / 1e12,
-                                    "ms": t_6 * 1e3, "frac_of_bf16_peak": f6 / t_6 / 1e12 / peak}
+                                    "ms": t_6 * 1e3, "frac_of_bf16_peak": f6 / t_6 / 1e12 / peak,
+                                    **per_clock(f6 / t_6 / 1e12, "d64", peak)}
         del q6, k6, v6, o6, l6
 
     if "causal" in extras:
@@ -460,7 +532,7 @@ def run_ours(args, ws, rank, local):
         oc = torch.empty_like(qc)
         lc = torch.empty((Bc, Hc, Nc), dtype=torch.float32, device=dev)
         n_c = max(5, min(args.steps, 50))
-        t_c = timed(lambda: fa.forward(qc, kc, vc, out=oc, lse=lc, causal=True), n_c, 2) / n_c
+        t_c = timed(lambda: fa.forward(qc, kc, vc, out=oc, lse=lc, causal=True), n_c, 2, key="causal_fwd") / n_c
         fc = 4.0 * Bc * Hc * d * Nc * (Nc + 1) / 2          # visible (query, key) pairs only
         del qc, kc, vc, oc, lc
         Bt, Ht, Nt = TRAIN["B"], TRAIN["H"], TRAIN["N"]
@@ -472,15 +544,17 @@ def run_ours(args, ws, rank, local):
         ws_b = torch.empty(fa.backward_workspace_size(Bt, Ht, Nt, d), dtype=torch.uint8, device=dev)
         n_tr = max(3, min(args.steps // 5, 20))
         t_cb = timed(lambda: fa.backward(qt, kt, vt, ot, lt, dot, dq=dq, dk=dk, dv=dv, workspace=ws_b, causal=True),
-                     n_tr, 1) / n_tr
+                     n_tr, 1, key="causal_bwd") / n_tr
         fcb = 2.5 * 4.0 * Bt * Ht * d * Nt * (Nt + 1) / 2
         extra["causal"] = {"flop_count": "4·B·H·d·N(N+1)/2 (visible pairs); backward 2.5x that",
                            "prefill_fwd": {"workload": "B=4 H=32 N=4096 d=128 bf16 causal",
                                            "tflops": fc / t_c / 1e12, "ms": t_c * 1e3,
-                                           "frac_of_bf16_peak": fc / t_c / 1e12 / peak},
+                                           "frac_of_bf16_peak": fc / t_c / 1e12 / peak,
+                                           **per_clock(fc / t_c / 1e12, "causal_fwd", peak)},
                            "train_bwd": {"workload": "B=2 H=16 N=8192 d=128 bf16 causal",
                                          "tflops": fcb / t_cb / 1e12, "ms": t_cb * 1e3,
-                                         "frac_of_bf16_peak": fcb / t_cb / 1e12 / peak}}
+                                         "frac_of_bf16_peak": fcb / t_cb / 1e12 / peak,
+                                         **per_clock(fcb / t_cb / 1e12, "causal_bwd", peak)}}
         del qt, kt, vt, dot, ot, lt, dq, dk, dv, ws_b
     fa.device_status()
 
@@ -502,6 +576,7 @@ def run_ours(args, ws, rank, local):
                    "inputs": "torch.randn (seeded Philox) on the device, rounded to bf16"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "per_clock": per_clock(achieved, "prefill", peak),
                      "kernel": "fwd_kernel<128, false>",
                      "traffic": traffic_for("fwd_prefill", ("fa_fwd.cu", "sm103.cuh"))},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -242,10 +242,16 @@ FA_API fa_status fa_decode_paged(const void* q, const void* k_cache, const void*
  *   FA_DECODE_STATIC_SCRATCH_BYTES (36 MiB) compiled into libfa.so, which every
  *   GPU that loads the library holds until the process exits.  If
  *   fa_decode_workspace_size(B, H, d, n_splits) is larger than that buffer the
- *   call returns FA_ERR_UNSUPPORTED and enqueues nothing (36 MiB covers, e.g.,
- *   B·H = 2048 heads with 32 splits at d = 128).
- *   The first call on a device looks up the buffer's device address with that
- *   device current; make that first call before any stream capture begins.
+ *   call returns FA_ERR_UNSUPPORTED and enqueues nothing (36 MiB covers up to
+ *   B·H = 2268 heads with 32 splits at d = 128).
+ *   The buffer belongs to the library's decode module.  Under CUDA's default
+ *   lazy module loading a device commits it (36 MiB) when it first runs any of
+ *   the library's decode entry points, not when libfa.so is loaded; a caller
+ *   that is about to reserve nearly all device memory should therefore make
+ *   one decode call (this one, say) first.  The first call on a device also
+ *   looks up the buffer's device address with that device current; make it
+ *   before any stream capture begins.  The address is looked up again after a
+ *   device reset gives the device a new context.
  *   Every call shares the one buffer, which keeps the last call's contents; each
  *   call rewrites every partial it reads, so nothing needs clearing.  Calls whose
  *   work overlaps on the GPU (other streams, other host threads) race on the

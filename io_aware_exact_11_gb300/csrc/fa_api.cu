@@ -31,6 +31,25 @@ __global__ void watchdog_selftest_kernel(unsigned int* err) {
     mbar_wait(&bar, 0, &abort_flag, err, (kKernSelftest << 8) | 1u);
   }
 }
+
+cudaError_t current_context(void** ctx) {
+  typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q != cudaDriverEntryPointSuccess) err = cudaErrorSymbolNotFound;
+    if (err == cudaSuccess) fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  if (fn == nullptr) return err != cudaSuccess ? err : cudaErrorSymbolNotFound;
+  CUcontext c = nullptr;
+  if (fn(&c) != CUDA_SUCCESS) return cudaErrorContextIsDestroyed;
+  *ctx = c;  // null while the runtime has not yet bound a context to this thread
+  return cudaSuccess;
+}
 }  // namespace fa
 
 namespace {
@@ -62,20 +81,26 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Device address of this device's watchdog word (looked up once per device).
+// Device address of this device's watchdog word, looked up once per device and
+// context: a device reset (a new primary context) triggers a fresh lookup.
 fa_status watchdog_ptr(unsigned int** out) {
   static std::mutex mu;
   static unsigned int* cache[64] = {};
+  static void* cache_ctx[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  void* ctx = nullptr;
+  if ((e = fa::current_context(&ctx)) != cudaSuccess) return cuda_fail(e, "cuCtxGetCurrent");
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev] == nullptr) {
+  if (cache[dev] == nullptr || ctx == nullptr || cache_ctx[dev] != ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_watchdog_word);
+    e = cudaGetSymbolAddress(&p, g_watchdog_word);  // binds the device's context if none was
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(watchdog)");
+    if ((e = fa::current_context(&ctx)) != cudaSuccess) return cuda_fail(e, "cuCtxGetCurrent");
     cache[dev] = static_cast<unsigned int*>(p);
+    cache_ctx[dev] = ctx;
   }
   *out = cache[dev];
   return FA_OK;

@@ -347,17 +347,23 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeStaticScr
 cudaError_t decode_static_scratch(void** out) {
   static std::mutex mu;
   static void* cache[64] = {};
+  static void* cache_ctx[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* ctx = nullptr;
+  if ((e = current_context(&ctx)) != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev] == nullptr) {
-    // Once per device, with that device current.
+  if (cache[dev] == nullptr || ctx == nullptr || cache_ctx[dev] != ctx) {
+    // Once per device (and again after a device reset gave it a new context),
+    // with that device current.
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess) return e;
+    if ((e = current_context(&ctx)) != cudaSuccess) return e;
     cache[dev] = p;
+    cache_ctx[dev] = ctx;
   }
   *out = cache[dev];
   return cudaSuccess;

@@ -118,7 +118,11 @@ cudaError_t launch_bwd_bf16(int d, const BwdParams& p, cudaStream_t s, int* laun
 
 // Size of the library-owned decode scratch (fa_decode_splitkv_noalloc).
 constexpr size_t kDecodeStaticScratchBytes = static_cast<size_t>(36) << 20;
-// Device address of that scratch on the current device (looked up once per device).
+// Device address of that scratch on the current device (looked up once per
+// device and context).
 cudaError_t decode_static_scratch(void** out);
+// The calling thread's current CUDA context (null if the runtime has not bound
+// one to the thread yet); keys the per-device caches of symbol addresses.
+cudaError_t current_context(void** ctx);
 
 }  // namespace fa

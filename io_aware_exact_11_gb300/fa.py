@@ -284,6 +284,19 @@ def choose_splits(B: int, Hq: int, Hkv: int, Nkv: int) -> int:
     return s
 
 
+def _check_decode_kv(q, k, v) -> int:
+    """k and v must be [B, H, N_kv, d] like q's B, H, d and share its dtype; returns N_kv."""
+    B, H, _, d = q.shape
+    if k.dim() != 4 or tuple(k.shape[:2]) != (B, H) or k.shape[3] != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("decode inputs must be contiguous")
+    return int(k.shape[2])
+
+
 def decode_splitkv(q, k, v, n_splits: int | None = None, scale: float | None = None, out=None, lse=None,
                    workspace=None, stream=None):
     """Split-KV decode: q [B,H,1,d] against k/v [B,H,Nkv,d]; returns (O, LSE).
@@ -293,10 +306,7 @@ def decode_splitkv(q, k, v, n_splits: int | None = None, scale: float | None = N
     B, H, one, d = q.shape
     if one != 1:
         raise ValueError("decode takes one query row per head")
-    Nkv = k.shape[2]
-    for t in (q, k, v):
-        if not t.is_contiguous():
-            raise ValueError("decode inputs must be contiguous")
+    Nkv = _check_decode_kv(q, k, v)
     if n_splits is None:
         n_splits = choose_splits(B, H, H, Nkv)
     if scale is None:
@@ -385,12 +395,14 @@ DECODE_STATIC_SCRATCH_BYTES = 36 << 20
 
 
 def decode_splitkv_noalloc(q, k, v, n_splits: int = 32, scale: float | None = None, out=None, lse=None,
-                           stream=None):
+                           return_lse: bool = True, stream=None):
     """Split-KV decode whose scratch is the library's fixed 36 MiB buffer.
 
     For callers that cannot provide device workspace (no allocator at decode
     time).  The library allocates nothing; `out` and `lse` are allocated here
-    only when not given.  Calls overlapping on the GPU race on the buffer.
+    only when not given (with ``return_lse=False`` and no `lse`, the library
+    writes no LSE and None is returned for it).  Calls overlapping on the GPU
+    race on the buffer.
     """
     torch = _torch()
     _check_cuda(q, k, v)
@@ -402,16 +414,14 @@ def decode_splitkv_noalloc(q, k, v, n_splits: int = 32, scale: float | None = No
     B, H, one, d = q.shape
     if one != 1:
         raise ValueError("decode takes one query row per head")
-    for t in (q, k, v):
-        if not t.is_contiguous():
-            raise ValueError("decode inputs must be contiguous")
+    Nkv = _check_decode_kv(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty((B, H, 1, d), dtype=q.dtype, device=q.device)
-    if lse is None:
+    if lse is None and return_lse:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, k.shape[2], d, _dtype_code(q), float(scale),
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nkv, d, _dtype_code(q), float(scale),
               int(n_splits), _stream_ptr(stream)))
     return out, lse
 
