@@ -333,51 +333,54 @@ def run_ours(args, ws, rank, local):
         barrier(ws)
         return e0.elapsed_time(e1) / 1e3
 
-    # ---------------- headline: prefill forward
-    B, H, N, d = PREFILL["B"], PREFILL["H"], PREFILL["N"], PREFILL["d"]
-    q, k, v = randn((B, H, N, d), 1), randn((B, H, N, d), 2), randn((B, H, N, d), 3)
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-
-    def step():
-        fa.forward(q, k, v, out=o, lse=lse)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    fa.device_status()
-    launches0 = fa.launch_count()
-    with ClockSampler(local) as clk:
-        el = timed(step, args.steps, 0, key="prefill")
-    launches = fa.launch_count() - launches0
-    fa.device_status()
-    el_max = max_over_ranks(el, ws, dev)
-    flops = fwd_flops(B, H, N, d)
-    value = flops * args.steps * ws / el_max / 1e12
-    per_launch = el / args.steps
-    achieved = flops / per_launch / 1e12
     peak = float(peaks["bf16_tflops"])
+    d = PREFILL["d"]
+    if not args.extras_only:
+        # ---------------- headline: prefill forward
+        B, H, N, d = PREFILL["B"], PREFILL["H"], PREFILL["N"], PREFILL["d"]
+        q, k, v = randn((B, H, N, d), 1), randn((B, H, N, d), 2), randn((B, H, N, d), 3)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
 
-    # ---------------- e2e: host buffers, copies inside the timed region
-    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        def step():
+            fa.forward(q, k, v, out=o, lse=lse)
 
-    def e2e_step():
-        # The C-ABI host-buffer entry point: q, k, v copied in and o, lse copied
-        # out every step, chunk by chunk, overlapped with the forward.
-        fa.forward_host(qh, kh, vh, out=oh, lse=lh)
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        fa.device_status()
+        launches0 = fa.launch_count()
+        with ClockSampler(local) as clk:
+            el = timed(step, args.steps, 0, key="prefill")
+        launches = fa.launch_count() - launches0
+        fa.device_status()
+        el_max = max_over_ranks(el, ws, dev)
+        flops = fwd_flops(B, H, N, d)
+        value = flops * args.steps * ws / el_max / 1e12
+        per_launch = el / args.steps
+        achieved = flops / per_launch / 1e12
 
-    e2e_steps = max(3, min(args.steps, 20))
-    el_e2e = max_over_ranks(timed(e2e_step, e2e_steps, 2), ws, dev)
-    h2d = 3 * q.numel() * q.element_size()
-    d2h = o.numel() * o.element_size() + lse.numel() * 4
-    e2e_value = flops * e2e_steps * ws / el_e2e / 1e12
-    del qh, kh, vh, oh, lh
+        # ---------------- e2e: host buffers, copies inside the timed region
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            # The C-ABI host-buffer entry point: q, k, v copied in and o, lse copied
+            # out every step, chunk by chunk, overlapped with the forward.
+            fa.forward_host(qh, kh, vh, out=oh, lse=lh)
+
+        e2e_steps = max(3, min(args.steps, 20))
+        el_e2e = max_over_ranks(timed(e2e_step, e2e_steps, 2), ws, dev)
+        h2d = 3 * q.numel() * q.element_size()
+        d2h = o.numel() * o.element_size() + lse.numel() * 4
+        e2e_value = flops * e2e_steps * ws / el_e2e / 1e12
+        del qh, kh, vh, oh, lh
 
     extra = {}
     extras = set() if args.quick else {x for x in args.extras.split(",") if x}
-    del q, k, v, o, lse
+    if not args.extras_only:
+        del q, k, v, o, lse
     if "long" in extras:
         # ---------------- long-context forward
         Bl, Hl, Nl = LONG["B"], LONG["H"], LONG["N"]
@@ -560,6 +563,9 @@ def run_ours(args, ws, rank, local):
 
     if rank != 0:
         return
+    if args.extras_only:
+        print(json.dumps({"extras_only": True, "extra": extra}), flush=True)
+        return
     cpu = None
     if ws == 1 and not args.no_cpu:
         cv, rows, secs = oracle_sample(args.cpu_seconds)
@@ -595,6 +601,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no long/decode/train extras)")
+    ap.add_argument("--extras-only", action="store_true",
+                    help="for profiling: measure only the listed extra workloads (no headline, no contract line)")
     ap.add_argument("--extras", default="long,decode,gqa,paged,train,causal,fp8,d64",
                     help="comma list of extra workloads measured after the headline")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
