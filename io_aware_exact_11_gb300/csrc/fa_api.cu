@@ -227,7 +227,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     return fail(FA_ERR_INVALID_ARG, "fa_forward: lse must be 4-byte aligned");
   if (causal && N_q > N_kv)
     return fail(FA_ERR_INVALID_ARG, "fa_forward: causal attention needs N_q <= N_kv (got %d > %d)", N_q, N_kv);
-  if (causal && (N_q + 255) / 256 > 65535)  // the causal grid puts the 256-row query blocks on its z axis
+  if (causal && (N_q + 255) / 256 > 65535)  // the causal grid puts the 256-row query blocks on its y axis
     return fail(FA_ERR_UNSUPPORTED, "fa_forward: causal attention needs N_q <= %d", 65535 * 256);
   const int esz = dtype == FA_BF16 ? 2 : 4;
   int64_t st[12];
@@ -862,7 +862,7 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   if (dtype != FA_BF16 || (d != 64 && d != 128))
     return fail(FA_ERR_UNSUPPORTED, "fa_backward: only bf16 with d = 64 or 128 is built");
   if (B > 65535 || H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_backward: B and H must be <= 65535");
-  if (causal && (N + 127) / 128 > 65535)  // the causal grid puts the 128-key tiles on its z axis
+  if (causal && (N + 127) / 128 > 65535)  // the causal grid puts the 128-key tiles on its y axis
     return fail(FA_ERR_UNSUPPORTED, "fa_backward: causal backward needs N <= %d", 65535 * 128);
   if (bad_scale(scale)) return fail(FA_ERR_INVALID_ARG, "fa_backward: scale must be finite and > 0");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||

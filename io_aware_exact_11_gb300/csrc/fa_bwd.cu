@@ -41,6 +41,8 @@
 // index) into the accumulator.
 // TMEM columns: Sᵀ 0..127 (then Pᵀ in 0..31 and 64..95), dPᵀ (then dQ_iᵀ) 128..255,
 // dV 256..383, dK 384..511.
+#include <algorithm>
+
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -180,11 +182,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Causal grids are (H, B, key tiles): key tile j meets T − j query tiles, so
-  // every head's longest tiles (small j) launch first.
-  const int j = p.causal ? blockIdx.z : blockIdx.x;
-  const int h = p.causal ? blockIdx.x : blockIdx.y;
-  const int b = p.causal ? blockIdx.y : blockIdx.z;
+  // Causal grids are (heads of a group, key tile, head group): key tile j meets
+  // T − j query tiles, so within a group of heads (small enough that their Q, dO
+  // and dQ stay in L2) every head's longest tiles (small j) launch first; the
+  // last group may be partly empty.
+  int j = static_cast<int>(blockIdx.x), h = static_cast<int>(blockIdx.y), b = static_cast<int>(blockIdx.z);
+  if (p.causal) {
+    const int fh = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
+    if (fh >= p.B * p.H) return;
+    j = static_cast<int>(blockIdx.y);
+    h = fh % p.H;
+    b = fh / p.H;
+  }
   const int64_t bh = static_cast<int64_t>(b) * p.H + h;
   const int T = (p.N + kTile - 1) / kTile;  // the last tile may be ragged
   const int i0 = p.causal ? j : 0;  // first query tile this key tile meets
@@ -555,7 +564,16 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, int* launches)
   if ((e = cudaFuncGetAttributes(&attr, bwd_main_kernel<D>)) != cudaSuccess) return e;
   if (attr.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
   const unsigned n_kt = (p.N + kTile - 1) / kTile;
-  const dim3 grid = p.causal ? dim3(p.H, p.B, n_kt) : dim3(n_kt, p.H, p.B);
+  dim3 grid(n_kt, p.H, p.B);
+  if (p.causal) {
+    // Heads per group: Q, dO (bf16) and the fp32 dQ accumulator about 32 MiB.
+    const int64_t bh = static_cast<int64_t>(p.B) * p.H;
+    const int64_t per_head = static_cast<int64_t>(p.N) * D * (2 + 2 + 4);
+    int64_t g = std::max<int64_t>(1, (int64_t{32} << 20) / per_head);
+    g = std::min(g, bh);
+    g = std::max(g, (bh + 65534) / 65535);  // the group count must fit the z axis
+    grid = dim3(static_cast<unsigned>(g), n_kt, static_cast<unsigned>((bh + g - 1) / g));
+  }
   bwd_main_kernel<D><<<grid, kThreads, kSmem, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

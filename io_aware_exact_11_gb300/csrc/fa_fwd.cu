@@ -45,10 +45,11 @@
 //
 // Causal mask (the lesson's §5 lab uses is_causal=True), bottom-right aligned:
 // row i sees keys j <= i + (N_kv − N_q).  A CTA streams only the key tiles its
-// last row can see; rows mask the rest of their diagonal tile with −∞, and
-// the heaviest query blocks of every head are scheduled first (the causal grid
-// is (H, B, query blocks), so all heads' longest blocks go out in the first
-// waves and the shortest ones fill the tail).
+// last row can see; rows mask the rest of their diagonal tile with −∞.  The
+// causal grid is (heads of a group, query-block rank, head group): heads are
+// taken in groups small enough that a group's K and V stay in L2, and within a
+// group the heaviest query blocks of every head go out first, so the short
+// blocks fill each group's tail and the last group's fill the grid's.
 //
 // FP8 (E4M3) variant, FlashAttention-3's addition noted in the lesson (§3.3) and
 // the interview notes (§四.5): Q, K, V arrive as E4M3 with per-tensor descale
@@ -71,6 +72,8 @@
 // final O/ℓ and LSE = m + ln ℓ are the same numbers in exact arithmetic; only
 // when the max really moves is O rescaled in TMEM by e^(m_old − m_new).
 #include <cuda_fp8.h>
+
+#include <algorithm>
 
 #include "fa_kernels.h"
 #include "sm103.cuh"
@@ -145,7 +148,9 @@ struct FwdWait {
   }
 };
 
-template <int D, bool FP8>
+// GROUPED: the causal launch's head-grouped grid (see the launcher); the
+// unmasked launches use the (query blocks, H, B) grid and GROUPED = false.
+template <int D, bool FP8, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   using W = FwdWait<D, FP8>;
   using L = FwdLayout<D, FP8>;
@@ -157,11 +162,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Causal grids are (H, B, query blocks), heaviest blocks of every head first.
-  const int mt = p.causal ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x);
+  // Grids are (query blocks, H, B); grouped (causal) grids are (heads of a
+  // group, query-block rank, head group), heaviest blocks first within each
+  // group, and the last group may be partly empty.
+  int mt = p.causal ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x);
+  int h = p.causal ? blockIdx.x : blockIdx.y;
+  int b = p.causal ? blockIdx.y : blockIdx.z;
+  if constexpr (GROUPED) {
+    const int fh = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
+    if (fh >= p.B * p.H) return;
+    mt = static_cast<int>(gridDim.y - 1 - blockIdx.y);
+    h = fh % p.H;
+    b = fh / p.H;
+  }
   const int m0 = mt * (kQT * kBM);
-  const int h = p.causal ? blockIdx.x : blockIdx.y;
-  const int b = p.causal ? blockIdx.y : blockIdx.z;
   const int off = p.Nkv - p.Nq;  // >= 0 whenever causal
   const int kv_end = p.causal ? min(p.Nkv, m0 + kQT * kBM + off) : p.Nkv;
   const int T = (kv_end + kBN - 1) / kBN;
@@ -515,12 +529,28 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 template <int D, bool FP8>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<D, FP8>;
-  cudaError_t e =
-      cudaFuncSetAttribute(fwd_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-  if (e != cudaSuccess) return e;
   const unsigned n_mt = (p.Nq + kQT * kBM - 1) / (kQT * kBM);
-  const dim3 grid = p.causal ? dim3(p.H, p.B, n_mt) : dim3(n_mt, p.H, p.B);
-  fwd_kernel<D, FP8><<<grid, kThreads, L::kSmem, stream>>>(p);
+  if (!p.causal) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel<D, FP8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return e;
+    fwd_kernel<D, FP8, false><<<dim3(n_mt, p.H, p.B), kThreads, L::kSmem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaError_t e =
+      cudaFuncSetAttribute(fwd_kernel<D, FP8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid;
+  {
+    // Heads per group: their K and V together about 32 MiB, a quarter of L2.
+    const int64_t bh = static_cast<int64_t>(p.B) * p.H;
+    const int64_t per_head = 2ll * p.Nkv * D * (FP8 ? 1 : 2);
+    int64_t g = std::max<int64_t>(1, (int64_t{32} << 20) / per_head);
+    g = std::min(g, bh);
+    g = std::max(g, (bh + 65534) / 65535);  // the group count must fit the z axis
+    grid = dim3(static_cast<unsigned>(g), n_mt, static_cast<unsigned>((bh + g - 1) / g));
+  }
+  fwd_kernel<D, FP8, true><<<grid, kThreads, L::kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
