@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # the forward kernel at the prefill shape (B=4 H=32 N=4096 d=128), one launch
-    "fwd_prefill": {"src": "469cb9fe0d1a4bab", "bytes": 402715392 + 121430016},
+    "fwd_prefill": {"src": "6f6f371f93e21cba", "bytes": 402853376 + 121230848},
     # the backward's main kernel at the training shape (B=2 H=16 N=8192 d=128), one launch
     "bwd_train": {"src": "517a4454ffb25174", "bytes": 404839168 + 223034368},
     # the split decode kernel, captured at B=8 (H=32 N_kv=8192 d=128); its traffic is
