@@ -46,10 +46,10 @@ NCU_TRAFFIC = {
     # the forward kernel at the prefill shape (B=4 H=32 N=4096 d=128), one launch
     "fwd_prefill": {"src": "6f6f371f93e21cba", "bytes": 402853376 + 121230848},
     # the backward's main kernel at the training shape (B=2 H=16 N=8192 d=128), one launch
-    "bwd_train": {"src": "517a4454ffb25174", "bytes": 404839168 + 223034368},
+    "bwd_train": {"src": "809505947237a1d5", "bytes": 404986368 + 222579456},
     # the split decode kernel, captured at B=8 (H=32 N_kv=8192 d=128); its traffic is
     # proportional to B, so it is stored here scaled to the B=64 launch
-    "decode_split": {"src": "71b693dc62ea91ee", "bytes": (1073836800 + 7016960) * 8},
+    "decode_split": {"src": "5296948a01a01d33", "bytes": (1073844224 + 6728960) * 8},
 }
 
 
@@ -587,7 +587,7 @@ def run_ours(args, ws, rank, local):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "per_clock": per_clock(achieved, "prefill"),
-                     "kernel": "fwd_kernel<128, false>",
+                     "kernel": "fwd_kernel<128, false, false>",
                      "traffic": traffic_for("fwd_prefill", ("fa_fwd.cu", "sm103.cuh"))},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
