@@ -118,6 +118,24 @@ def test_causal_prefill_full_size_sampled():
         assert max_abs(cpu64(lse[b, h])[rows], rl) <= TOL_LSE_BF16
 
 
+def test_causal_forward_partial_head_group():
+    """The causal grid takes heads in groups whose K and V fit a share of L2
+    (8 heads at N_kv = 8192, d = 128); with 11 heads the second group is partly
+    empty.  Sampled rows of a head in each group, against the oracle."""
+    B, H, N, d = 1, 11, 8192, 128
+    host, dev = make_qkv(28, B, H, N, N, d, "bf16")
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward(dev["q"], dev["k"], dev["v"], scale, causal=True)
+    fa.device_status()
+    rng = np.random.default_rng(12)
+    for h in (0, 7, 8, 10):
+        rows = np.concatenate([[0, 255, 256, N - 1], np.sort(rng.choice(N, 24, replace=False))])
+        ro, rl = oracle.attention_rows(f64(host["q"][0, h], "bf16"), f64(host["k"][0, h], "bf16"),
+                                       f64(host["v"][0, h], "bf16"), scale, rows, causal=True)
+        assert max_abs(cpu64(o[0, h])[rows], ro) <= TOL_O_BF16, h
+        assert max_abs(cpu64(lse[0, h])[rows], rl) <= TOL_LSE_BF16, h
+
+
 def _bwd(seed, B, H, N, heads=None, d=128):
     host, dev = make_qkv(seed, B, H, N, N, d, "bf16", with_do=True)
     scale = 1 / math.sqrt(d)
@@ -139,6 +157,13 @@ def test_causal_backward(B, H, N):
 @pytest.mark.parametrize("B,H,N", [(1, 2, 384), (1, 1, 300)])
 def test_causal_backward_head_dim_64(B, H, N):
     _bwd(27, B, H, N, d=64)
+
+
+def test_causal_backward_partial_head_group():
+    """The causal backward grid takes heads in groups whose Q, dO and fp32 dQ
+    fit a share of L2 (8 heads at N = 4096, d = 128); with 9 heads the second
+    group holds one head.  The first head and the lone one, against the oracle."""
+    _bwd(29, 1, 9, 4096, heads=[(0, 0), (0, 8)])
 
 
 @pytest.mark.slow
