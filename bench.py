@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # the forward kernel at the prefill shape (B=4 H=32 N=4096 d=128), one launch
-    "fwd_prefill": {"src": "6f6f371f93e21cba", "bytes": 402853376 + 121230848},
+    "fwd_prefill": {"src": "ae2e554c1ff89acb", "bytes": 402780672 + 121440256},
     # the backward's main kernel at the training shape (B=2 H=16 N=8192 d=128), one launch
     "bwd_train": {"src": "809505947237a1d5", "bytes": 404986368 + 222579456},
     # the split decode kernel, captured at B=8 (H=32 N_kv=8192 d=128); its traffic is

@@ -129,10 +129,11 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 // Barrier waits with the polling loop inlined or out of line.  Which one gives
 // the better code differs by instantiation (measured on GB300: inlined waits
-// cost bf16 d = 128 about 5 % and gain 5 % at E4M3 and 8 % at d = 64).
-template <int D, bool FP8>
+// cost the unmasked bf16 d = 128 instance about 5 % and gain 5 % at E4M3, 8 %
+// at d = 64 and 2–3 % for the causal head-grouped instance).
+template <int D, bool FP8, bool GROUPED = false>
 struct FwdWait {
-  static constexpr bool kInline = FP8 || D == 64;
+  static constexpr bool kInline = FP8 || D == 64 || GROUPED;
   __device__ static __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned int* err, unsigned int code) {
     if constexpr (kInline)
@@ -152,7 +153,7 @@ struct FwdWait {
 // unmasked launches use the (query blocks, H, B) grid and GROUPED = false.
 template <int D, bool FP8, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
-  using W = FwdWait<D, FP8>;
+  using W = FwdWait<D, FP8, GROUPED>;
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
