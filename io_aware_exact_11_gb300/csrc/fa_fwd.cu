@@ -31,7 +31,8 @@
 // Warp roles (320 threads):
 //   warp 0       TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, … through
 //                a shared-memory ring (5 slots at d = 128 bf16)
-//   warp 1       TMEM owner and MMA issuer (one thread)
+//   warp 1       TMEM owner and MMA issuer (one thread, or one elected lane of
+//                the converged warp: kUniformIssue)
 //   warps 2..5   softmax / rescale / epilogue of Q_0 (warp w reads TMEM lanes 32·(w%4)…)
 //   warps 6..9   the same for Q_1
 // TMEM: S_0 / P̃_0 (columns 0..127), S_1 / P̃_1 (128..255), O_0 (256..), O_1 (384..).
@@ -119,6 +120,13 @@ struct FwdBars {
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernFwd << 8) | s; }
 
+// True on one lane of a converged warp (elect.sync).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
 // Four fp32 values -> four E4M3 bytes (round to nearest even, saturating), the
 // first value in the lowest byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -127,13 +135,19 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// Barrier waits with the polling loop inlined or out of line.  Which one gives
-// the better code differs by instantiation (measured on GB300: inlined waits
-// cost the unmasked bf16 d = 128 instance about 5 % and gain 5 % at E4M3, 8 %
-// at d = 64 and 2–3 % for the causal head-grouped instance).
+// Barrier waits with the polling loop inlined or out of line, and how the MMA
+// warp issues.  Which gives the better code differs by instantiation (measured
+// on GB300: inlined waits cost the unmasked bf16 d = 128 instance about 5 % and
+// gain 5 % at E4M3, 8 % at d = 64 and 2–3 % for the causal head-grouped
+// instance).  kUniformIssue: the MMA warp runs its loop on all 32 lanes, so
+// shared-memory descriptors are warp-uniform values, and one elected lane
+// issues; a single issuing thread instead loses issue slots to the softmax
+// warps of its sub-partition (+7 % at d = 64, +4 % causal, +6.5 % E4M3, but
+// −3 % for the unmasked bf16 d = 128 instance, which keeps one thread).
 template <int D, bool FP8, bool GROUPED = false>
 struct FwdWait {
   static constexpr bool kInline = FP8 || D == 64 || GROUPED;
+  static constexpr bool kUniformIssue = kInline;
   __device__ static __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned int* err, unsigned int code) {
     if constexpr (kInline)
@@ -237,13 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // One thread, or (kUniformIssue) the whole warp with one elected lane
+    // issuing; every lane then takes the same wait results.
+    constexpr bool kUni = W::kUniformIssue;
+    const bool leader = kUni ? elect_one() : true;
+    auto agree = [](bool v) { return kUni ? static_cast<bool>(__all_sync(0xffffffffu, v)) : v; };
+    if (kUni || lane == 0) {
       constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t kIdescO = FP8 ? idesc_e4m3_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
       const uint32_t sQ = smem_u32(smem + L::kQ);
       const uint32_t sR = smem_u32(smem + L::kR);
       auto ring_wait = [&](int t, unsigned int where) -> bool {
-        return W::wait(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, abort_flag, p.err, site(where));
+        return agree(W::wait(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, abort_flag, p.err, site(where)));
       };
       auto issue_s = [&](int i, uint32_t kb) {  // S_i = Q_i K_jᵀ
         const uint32_t qb = sQ + i * L::kSlot;
@@ -251,18 +270,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         for (int kk = 0; kk < D / L::kStepK; ++kk) {
           const uint32_t o = (kk >> 2) * kTileBytes + (kk & 3) * 32;
           const uint64_t ad = sdesc_sw128(qb + o, 16, 1024), bd = sdesc_sw128(kb + o, 16, 1024);
-          if (FP8)
-            mma_e4m3_ss(tmem + i * kBN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-          else
-            mma_bf16_ss(tmem + i * kBN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+          if (leader) {
+            if (FP8)
+              mma_e4m3_ss(tmem + i * kBN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            else
+              mma_bf16_ss(tmem + i * kBN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+          }
         }
       };
-      bool ok = W::wait(&bars->q_full, 0, abort_flag, p.err, site(5)) && ring_wait(0, 6);
+      bool ok = agree(W::wait(&bars->q_full, 0, abort_flag, p.err, site(5))) && ring_wait(0, 6);
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < kQT; ++i) {
           issue_s(i, sR);
-          mma_commit(&bars->s_full[i]);
+          if (leader) mma_commit(&bars->s_full[i]);
         }
       }
       for (int j = 0; ok && j < T; ++j) {
@@ -272,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         const bool next = j + 1 < T;
         const uint32_t kb = sR + ((tv + 1) % L::kRing) * L::kSlot;
         for (int i = 0; i < kQT && ok; ++i) {
-          if (!(ok = W::wait(FP8 ? &bars->p_half[i] : &bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
+          if (!(ok = agree(W::wait(FP8 ? &bars->p_half[i] : &bars->p_full[i], j & 1, abort_flag, p.err, site(4)))))
+            break;
           if (i == 0 && next && !(ok = ring_wait(tv + 1, 6))) break;
           tc_fence_after();
           // O_i += P̃_i V_j: A = P̃_i from S_i's TMEM columns (32 bytes of keys = 8
@@ -281,23 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int kk = 0; kk < kBN / L::kStepK; ++kk) {
             if (FP8 && kk == kHalf) {  // the second half of P̃_i
-              if (!(ok = W::wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4)))) break;
+              if (!(ok = agree(W::wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4))))) break;
               tc_fence_after();
             }
             const uint64_t bd = sdesc_sw128(vb + kk * L::kStepK * 128, kTileBytes, 1024);
             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-            if (FP8)
-              mma_e4m3_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
-            else
-              mma_bf16_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
+            if (leader) {
+              if (FP8)
+                mma_e4m3_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
+              else
+                mma_bf16_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
+            }
           }
           if (FP8 && !ok) break;
           if (next) issue_s(i, kb);
-          mma_commit(&bars->s_full[i]);
+          if (leader) mma_commit(&bars->s_full[i]);
         }
       }
       if (*abort_flag) {
-        mma_commit(&bars->drain);
+        if (leader) mma_commit(&bars->drain);
         W::drain(&bars->drain, 0, 200000000ull);
       }
     }
