@@ -90,6 +90,13 @@ static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernBwd << 8) | s; }
 
+// True on one lane of a converged warp (elect.sync).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
 // Adds 32 columns of dQᵀ (this lane's head dim, columns cbase … cbase+31) into
 // the fp32 accumulator rows: per block of four columns, a 4 × 4 exchange among
 // lanes 4g … 4g+3 gives lane 4g + r4 column c0 + r4 for head dims 4g … 4g+3,
@@ -272,7 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop, so shared-memory descriptors are warp-
+    // uniform values, and one elected lane issues: a single issuing thread
+    // loses issue slots to the compute and drain warps of its sub-partition
+    // (+1.8 % measured on GB300).  Every lane takes the same wait results.
+    {
+      const bool leader = elect_one();
+      auto agree = [](bool v) { return static_cast<bool>(__all_sync(0xffffffffu, v)); };
       constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // Sᵀ, dPᵀ
       constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV (A in TMEM), dK
       // dQᵀ keeps M = 128 for every D: with D = 64 its A operand (K read MN-major)
@@ -286,13 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024), kIdescKK,
-                      kk > 0 ? 1u : 0u);
+          if (leader)
+            mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024), kIdescKK,
+                        kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->s_full);
+        if (leader) mma_commit(&bars->s_full);
       };
-      bool ok = mbar_wait_inl(&bars->kv_full, 0, abort_flag, p.err, site(2)) &&
-                mbar_wait_inl(&bars->q_full[0], 0, abort_flag, p.err, site(3));
+      bool ok = agree(mbar_wait_inl(&bars->kv_full, 0, abort_flag, p.err, site(2))) &&
+                agree(mbar_wait_inl(&bars->q_full[0], 0, abort_flag, p.err, site(3)));
       if (ok) {
         tc_fence_after();
         issue_st(0);
@@ -302,48 +316,53 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         const uint32_t dob = sDO + (it & 1) * kOpBytes;
         const uint32_t qb = sQ + (it & 1) * kOpBytes;
         // dPᵀ_i = V_j dO_iᵀ into columns that held dQ_{i−1}: wait until it is drained.
-        if (!(ok = mbar_wait_inl(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(4)))) break;
+        if (!(ok = agree(mbar_wait_inl(&bars->dq_free, ph ^ 1, abort_flag, p.err, site(4))))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), kIdescKK,
-                      kk > 0 ? 1u : 0u);
+          if (leader)
+            mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), kIdescKK,
+                        kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->dp_full);
+        if (leader) mma_commit(&bars->dp_full);
         // dV += Pᵀ dO_i with Pᵀ (bf16 pairs) read from TMEM columns 0..63.
-        if (!(ok = mbar_wait_inl(&bars->p_ready, ph, abort_flag, p.err, site(5)))) break;
+        if (!(ok = agree(mbar_wait_inl(&bars->p_ready, ph, abort_flag, p.err, site(5))))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                      sdesc_sw128(dob + kk * 2048, kTileBytes, 1024), kIdescKM,
-                      (it > 0 || kk > 0) ? 1u : 0u);
+          if (leader)
+            mma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                        sdesc_sw128(dob + kk * 2048, kTileBytes, 1024), kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
         // Sᵀ_{i+1} overwrites Pᵀ_i, which the dV MMAs above read first (in order).
         if (it + 1 < nT) {
-          if (!(ok = mbar_wait_inl(&bars->q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort_flag, p.err, site(6)))) break;
+          if (!(ok = agree(mbar_wait_inl(&bars->q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort_flag, p.err,
+                                         site(6)))))
+            break;
           tc_fence_after();
           issue_st(it + 1);
         }
-        if (!(ok = mbar_wait_inl(&bars->ds_ready, ph, abort_flag, p.err, site(7)))) break;
+        if (!(ok = agree(mbar_wait_inl(&bars->ds_ready, ph, abort_flag, p.err, site(7))))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {  // dK += dSᵀ Q_i
-          mma_bf16_ss(tmem + kColDK, sdesc_sw128(sDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
-                      sdesc_sw128(qb + kk * 2048, kTileBytes, 1024), kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
+          if (leader)
+            mma_bf16_ss(tmem + kColDK, sdesc_sw128(sDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
+                        sdesc_sw128(qb + kk * 2048, kTileBytes, 1024), kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {  // dQ_iᵀ = K_jᵀ dSᵀ (A = K_j and B = dSᵀ, both MN-major)
-          mma_bf16_ss(tmem + kColDP, sdesc_sw128(sK + kk * 2048, kTileBytes, 1024),
-                      sdesc_sw128(sDST + kk * 2048, kTileBytes, 1024), kIdescMM, kk > 0 ? 1u : 0u);
+          if (leader)
+            mma_bf16_ss(tmem + kColDP, sdesc_sw128(sK + kk * 2048, kTileBytes, 1024),
+                        sdesc_sw128(sDST + kk * 2048, kTileBytes, 1024), kIdescMM, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->dq_full);
-        mma_commit(&bars->ds_free);
-        mma_commit(&bars->q_empty[it & 1]);
+        if (leader) mma_commit(&bars->dq_full);
+        if (leader) mma_commit(&bars->ds_free);
+        if (leader) mma_commit(&bars->q_empty[it & 1]);
       }
-      mma_commit(&bars->acc_done);
+      if (leader) mma_commit(&bars->acc_done);
       if (*abort_flag) {
-        mma_commit(&bars->drain);
+        if (leader) mma_commit(&bars->drain);
         mbar_wait_drain_inl(&bars->drain, 0, 200000000ull);
       }
     }
