@@ -31,8 +31,8 @@
 // Warp roles (320 threads):
 //   warp 0       TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, … through
 //                a shared-memory ring (5 slots at d = 128 bf16)
-//   warp 1       TMEM owner and MMA issuer (one thread, or one elected lane of
-//                the converged warp: kUniformIssue)
+//   warp 1       TMEM owner and MMA issuer (the converged warp, one elected lane
+//                issuing)
 //   warps 2..5   softmax / rescale / epilogue of Q_0 (warp w reads TMEM lanes 32·(w%4)…)
 //   warps 6..9   the same for Q_1
 // TMEM: S_0 / P̃_0 (columns 0..127), S_1 / P̃_1 (128..255), O_0 (256..), O_1 (384..).
@@ -135,39 +135,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// Barrier waits with the polling loop inlined or out of line, and how the MMA
-// warp issues.  Which gives the better code differs by instantiation (measured
-// on GB300: inlined waits cost the unmasked bf16 d = 128 instance about 5 % and
-// gain 5 % at E4M3, 8 % at d = 64 and 2–3 % for the causal head-grouped
-// instance).  kUniformIssue: the MMA warp runs its loop on all 32 lanes, so
-// shared-memory descriptors are warp-uniform values, and one elected lane
-// issues; a single issuing thread instead loses issue slots to the softmax
-// warps of its sub-partition (+7 % at d = 64, +4 % causal, +6.5 % E4M3, but
-// −3 % for the unmasked bf16 d = 128 instance, which keeps one thread).
-template <int D, bool FP8, bool GROUPED = false>
-struct FwdWait {
-  static constexpr bool kInline = FP8 || D == 64 || GROUPED;
-  static constexpr bool kUniformIssue = kInline;
-  __device__ static __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              unsigned int* err, unsigned int code) {
-    if constexpr (kInline)
-      return mbar_wait_inl(bar, parity, abort_flag, err, code);
-    else
-      return mbar_wait(bar, parity, abort_flag, err, code);
-  }
-  __device__ static __forceinline__ bool drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-    if constexpr (kInline)
-      return mbar_wait_drain_inl(bar, parity, timeout_ns);
-    else
-      return mbar_wait_drain(bar, parity, timeout_ns);
-  }
-};
-
 // GROUPED: the causal launch's head-grouped grid (see the launcher); the
 // unmasked launches use the (query blocks, H, B) grid and GROUPED = false.
 template <int D, bool FP8, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
-  using W = FwdWait<D, FP8, GROUPED>;
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -235,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       for (int t = 0; t < 2 * T; ++t) {
         const int slot = t % L::kRing;
         const uint32_t u = t / L::kRing;
-        if (!W::wait(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
+        if (!mbar_wait_inl(&bars->r_empty[slot], (u & 1) ^ 1, abort_flag, p.err, site(1))) break;
         mbar_arrive_expect_tx(&bars->r_full[slot], L::kSlot);
         const CUtensorMap* tm = (t & 1) ? &p.tm_v : &p.tm_k;
         for (int kb = 0; kb < L::kNKB; ++kb)
@@ -244,25 +215,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         ++issued;
       }
       if (*abort_flag) {
-        W::drain(&bars->q_full, 0, 200000000ull);
+        mbar_wait_drain_inl(&bars->q_full, 0, 200000000ull);
         for (int t = (issued > L::kRing ? issued - L::kRing : 0); t < issued; ++t)
-          W::drain(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, 200000000ull);
+          mbar_wait_drain_inl(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, 200000000ull);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread, or (kUniformIssue) the whole warp with one elected lane
-    // issuing; every lane then takes the same wait results.
-    constexpr bool kUni = W::kUniformIssue;
-    const bool leader = kUni ? elect_one() : true;
-    auto agree = [](bool v) { return kUni ? static_cast<bool>(__all_sync(0xffffffffu, v)) : v; };
-    if (kUni || lane == 0) {
+    // The whole warp runs the loop, so shared-memory descriptors are warp-
+    // uniform values, and one elected lane issues; a single issuing thread
+    // loses issue slots to the softmax warps of its sub-partition.  Every lane
+    // takes the same wait results.  (Measured on GB300, together with the
+    // inlined barrier waits: +4 % at the prefill shape, +7 % at d = 64, +6 %
+    // for E4M3 and the causal mask; either change alone cost the unmasked bf16
+    // d = 128 instance 3–5 %.)
+    const bool leader = elect_one();
+    auto agree = [](bool v) { return static_cast<bool>(__all_sync(0xffffffffu, v)); };
+    {
       constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t kIdescO = FP8 ? idesc_e4m3_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
       const uint32_t sQ = smem_u32(smem + L::kQ);
       const uint32_t sR = smem_u32(smem + L::kR);
       auto ring_wait = [&](int t, unsigned int where) -> bool {
-        return agree(W::wait(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, abort_flag, p.err, site(where)));
+        return agree(mbar_wait_inl(&bars->r_full[t % L::kRing], (t / L::kRing) & 1, abort_flag, p.err, site(where)));
       };
       auto issue_s = [&](int i, uint32_t kb) {  // S_i = Q_i K_jᵀ
         const uint32_t qb = sQ + i * L::kSlot;
@@ -278,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           }
         }
       };
-      bool ok = agree(W::wait(&bars->q_full, 0, abort_flag, p.err, site(5))) && ring_wait(0, 6);
+      bool ok = agree(mbar_wait_inl(&bars->q_full, 0, abort_flag, p.err, site(5))) && ring_wait(0, 6);
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < kQT; ++i) {
@@ -293,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         const bool next = j + 1 < T;
         const uint32_t kb = sR + ((tv + 1) % L::kRing) * L::kSlot;
         for (int i = 0; i < kQT && ok; ++i) {
-          if (!(ok = agree(W::wait(FP8 ? &bars->p_half[i] : &bars->p_full[i], j & 1, abort_flag, p.err, site(4)))))
+          if (!(ok = agree(mbar_wait_inl(FP8 ? &bars->p_half[i] : &bars->p_full[i], j & 1, abort_flag, p.err, site(4)))))
             break;
           if (i == 0 && next && !(ok = ring_wait(tv + 1, 6))) break;
           tc_fence_after();
@@ -303,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int kk = 0; kk < kBN / L::kStepK; ++kk) {
             if (FP8 && kk == kHalf) {  // the second half of P̃_i
-              if (!(ok = agree(W::wait(&bars->p_full[i], j & 1, abort_flag, p.err, site(4))))) break;
+              if (!(ok = agree(mbar_wait_inl(&bars->p_full[i], j & 1, abort_flag, p.err, site(4))))) break;
               tc_fence_after();
             }
             const uint64_t bd = sdesc_sw128(vb + kk * L::kStepK * 128, kTileBytes, 1024);
@@ -322,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       }
       if (*abort_flag) {
         if (leader) mma_commit(&bars->drain);
-        W::drain(&bars->drain, 0, 200000000ull);
+        mbar_wait_drain_inl(&bars->drain, 0, 200000000ull);
       }
     }
   } else {
@@ -339,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      ok = W::wait(&bars->s_full[qt], j & 1, abort_flag, p.err, site(8));
+      ok = mbar_wait_inl(&bars->s_full[qt], j & 1, abort_flag, p.err, site(8));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       // S_1(j) is complete, so K_j and V_{j−1} have been read by both tiles.
       if (releaser) {
@@ -457,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       // Head dim 64: each thread writes its 128-byte row directly (measured
       // faster here than staging through shared memory).
       if (ok) {
-        ok = W::wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
+        ok = mbar_wait_inl(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
         if (__all_sync(0xffffffffu, ok)) {
           tc_fence_after();
           const float inv = p.o_scale / l_run;
@@ -494,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       // store is then skipped), so none waits for a warp that left.
       bool eok = false;
       if (ok) {
-        ok = W::wait(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
+        ok = mbar_wait_inl(&bars->s_full[qt], T & 1, abort_flag, p.err, site(10));
         eok = __all_sync(0xffffffffu, ok);
       }
       const int grow = m0 + qt * kBM + row;
