@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_f32.cu", "fa_decode.cu", "fa_decode_tc.cu", "fa_bwd.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_d64.cu", "fa_fwd_f32.cu", "fa_decode.cu", "fa_decode_tc.cu", "fa_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -251,8 +251,11 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     memset(&p, 0, sizeof(p));
     fa_status r;
     if ((r = make_map(&p.tm_q, q, B, H, N_q, d, st[0], st[1], st[2], "q")) != FA_OK) return r;
-    if ((r = make_map(&p.tm_k, k, B, H, N_kv, d, st[3], st[4], st[5], "k")) != FA_OK) return r;
-    if ((r = make_map(&p.tm_v, v, B, H, N_kv, d, st[6], st[7], st[8], "v")) != FA_OK) return r;
+    // The unmasked d = 64 kernel streams 64-key tiles; every other case 128.
+    const bool d64_tiles = d == 64 && !causal;
+    const int kv_rows = d64_tiles ? 64 : 128;
+    if ((r = make_map(&p.tm_k, k, B, H, N_kv, d, st[3], st[4], st[5], "k", kv_rows)) != FA_OK) return r;
+    if ((r = make_map(&p.tm_v, v, B, H, N_kv, d, st[6], st[7], st[8], "v", kv_rows)) != FA_OK) return r;
     if ((r = make_map(&p.tm_o, o, B, H, N_q, d, st[9], st[10], st[11], "o")) != FA_OK) return r;
     if ((r = watchdog_ptr(&p.err)) != FA_OK) return r;
     p.o = o;
@@ -267,7 +270,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
     p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal;
     p.o_scale = 1.f;
-    cudaError_t e = fa::launch_fwd_bf16(d, p, s);
+    cudaError_t e = d64_tiles ? fa::launch_fwd_d64_tiles(4, p, s) : fa::launch_fwd_bf16(d, p, s);
     if (e != cudaSuccess) return cuda_fail(e, "fa_forward launch");
     return check_launch("fa_forward", 1);
   }

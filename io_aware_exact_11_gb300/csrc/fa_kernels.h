@@ -107,6 +107,9 @@ struct BwdParams {
 };
 
 cudaError_t launch_fwd_bf16(int d, const FwdParams& p, cudaStream_t s);
+// Unmasked bf16 forward at d = 64 with 3 or 4 query tiles of 128 rows per CTA
+// (fa_fwd_d64.cu); K/V maps with 64-row boxes.
+cudaError_t launch_fwd_d64_tiles(int query_tiles, const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_fp8(int d, const FwdParams& p, cudaStream_t s);  // E4M3 Q/K/V, bf16 O
 cudaError_t launch_fwd_f32(int d, const FwdF32Params& p, cudaStream_t s);
 cudaError_t launch_decode_bf16(int d, const DecodeParams& p, cudaStream_t s);
