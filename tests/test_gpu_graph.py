@@ -44,10 +44,10 @@ def _refill(dst, seed, name, dtype="bf16"):
     dst.copy_(src)
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_forward_replay_matches_eager(causal):
+@pytest.mark.parametrize("d,causal", [(128, False), (128, True), (64, False)])
+def test_forward_replay_matches_eager(d, causal):
     import torch
-    B, H, N, d = 2, 3, 300, 128
+    B, H, N = 2, 3, 300
     _, dev = make_qkv(71, B, H, N, N, d, "bf16")
     q, k, v = dev["q"], dev["k"], dev["v"]
     o = torch.empty_like(q)

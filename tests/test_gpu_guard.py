@@ -41,6 +41,11 @@ def _check(*gs):
     (2, 2, 1, 129, 128, False),
     (1, 2, 200, 457, 128, True),
     (1, 5, 333, 333, 64, True),
+    # head dim 64 without the mask (four 128-row query tiles per CTA, 64-key tiles):
+    # a ragged last CTA, one with three query tiles wholly past N_q, exactly one key tile
+    (1, 5, 333, 271, 64, False),
+    (2, 3, 1, 1, 64, False),
+    (2, 3, 700, 64, 64, False),
 ])
 def test_forward_writes_stay_inside_o_and_lse(B, H, Nq, Nkv, d, causal):
     import torch

@@ -135,10 +135,12 @@ def test_forward_bf16_rising_scores_rescale_mid_sequence(d, causal):
         assert max_abs(cpu64(lse[0, h]), ref_lse) <= TOL_LSE_BF16 * max(1.0, float(np.abs(ref_lse).max()) / 8), h
 
 
-def test_forward_strided_inputs():
-    """Q/K/V/O as [B, N, H, d] buffers viewed as [B, H, N, d]."""
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_strided_inputs(d):
+    """Q/K/V/O as [B, N, H, d] buffers viewed as [B, H, N, d] (at d = 64 the
+    four-query-tile kernel, whose O leaves by direct stores through the strides)."""
     import torch
-    B, H, N, d = 2, 3, 256, 128
+    B, H, N = 2, 3, 256
     host, dev = make_qkv(3, B, H, N, N, d, "bf16")
     qs, ks, vs = (dev[n].transpose(1, 2).contiguous().transpose(1, 2) for n in ("q", "k", "v"))
     assert not qs.is_contiguous()
@@ -148,17 +150,19 @@ def test_forward_strided_inputs():
     assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
 
-def test_forward_deterministic():
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_deterministic(d):
     import torch
-    _, dev = make_qkv(2, 1, 4, 512, 512, 128, "bf16")
+    _, dev = make_qkv(2, 1, 4, 512, 512, d, "bf16")
     o1, l1 = fa.forward(dev["q"], dev["k"], dev["v"])
     o2, l2 = fa.forward(dev["q"], dev["k"], dev["v"])
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_values_all_ones_give_ones():
+@pytest.mark.parametrize("d", [64, 128])
+def test_values_all_ones_give_ones(d):
     import torch
-    B, H, N, d = 1, 2, 300, 128
+    B, H, N = 1, 2, 300
     _, dev = make_qkv(4, B, H, N, N, d, "bf16")
     ones = torch.ones_like(dev["v"])
     o, _ = fa.forward(dev["q"], dev["k"], ones)
