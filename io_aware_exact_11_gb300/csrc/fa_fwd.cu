@@ -137,9 +137,13 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 // GROUPED: the causal launch's head-grouped grid (see the launcher); the
 // unmasked launches use the (query blocks, H, B) grid and GROUPED = false.
+// The launcher pairs the two one to one, so the mask is a compile-time choice
+// here (measured on GB300: +2.3 % at the unmasked prefill shape, +1.5 % causal
+// over reading p.causal).
 template <int D, bool FP8, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D, FP8>;
+  constexpr bool kCausal = GROUPED;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -151,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
   // Grids are (query blocks, H, B); grouped (causal) grids are (heads of a
   // group, query-block rank, head group), heaviest blocks first within each
   // group, and the last group may be partly empty.
-  int mt = p.causal ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x);
-  int h = p.causal ? blockIdx.x : blockIdx.y;
-  int b = p.causal ? blockIdx.y : blockIdx.z;
+  int mt = kCausal ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x);
+  int h = kCausal ? blockIdx.x : blockIdx.y;
+  int b = kCausal ? blockIdx.y : blockIdx.z;
   if constexpr (GROUPED) {
     const int fh = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
     if (fh >= p.B * p.H) return;
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
   }
   const int m0 = mt * (kQT * kBM);
   const int off = p.Nkv - p.Nq;  // >= 0 whenever causal
-  const int kv_end = p.causal ? min(p.Nkv, m0 + kQT * kBM + off) : p.Nkv;
+  const int kv_end = kCausal ? min(p.Nkv, m0 + kQT * kBM + off) : p.Nkv;
   const int T = (kv_end + kBN - 1) / kBN;
 
   if (threadIdx.x == 0) {
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         }
       }
       int kv_valid = p.Nkv - j * kBN;
-      if (p.causal) kv_valid = min(kv_valid, m0 + qt * kBM + row + off + 1 - j * kBN);
+      if (kCausal) kv_valid = min(kv_valid, m0 + qt * kBM + row + off + 1 - j * kBN);
       if (kv_valid < kBN) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
