@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # time; a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # the forward kernel at the prefill shape (B=4 H=32 N=4096 d=128), one launch
-    "fwd_prefill": {"src": "17032b2c45c14a3f", "bytes": 402764032 + 115732736},
+    "fwd_prefill": {"src": "64dd18fcd837069e", "bytes": 402994176 + 114389760},
     # the backward's main kernel at the training shape (B=2 H=16 N=8192 d=128), one launch
     "bwd_train": {"src": "a90661bb6cd3e299", "bytes": 404845568 + 222076416},
     # the split decode kernel, captured at B=8 (H=32 N_kv=8192 d=128); its traffic is
