@@ -58,14 +58,14 @@
 // bytes per k-step), P̃ is stored as E4M3 (lazy rescaling keeps it <= 256, inside
 // E4M3's ±448) and ℓ sums the unrounded fp32 values; O leaves as bf16.
 //
-// E4M3 hands P̃ over in two halves: a softmax warp whose rows keep their
-// reference max signals p_half once P̃ of the first 64 keys is in TMEM, and the
-// MMA warp issues that half of P̃_iV_j while the second half's exponentials are
-// still running (a warp that rescales O signals both halves after the rescale,
-// so no P̃V MMA reads O before it).  The MMAs and their order are unchanged, so
-// the results are identical.  Measured on GB300: E4M3 +6–9 %; the bf16
-// instances lost 3 % (d = 64) and 16 % (d = 128) with the same split, so they
-// hand over the whole tile at once.
+// P̃ goes over in two halves: a softmax warp whose rows keep their reference
+// max signals p_half once P̃ of the first 64 keys is in TMEM, and the MMA warp
+// issues that half of P̃_iV_j while the second half's exponentials are still
+// running (a warp that rescales O signals both halves after the rescale, so no
+// P̃V MMA reads O before it).  The MMAs and their order are unchanged, so the
+// results are identical.  Measured on GB300 with the converged MMA warp: E4M3
+// +10 %, bf16 +2 % at the prefill shape and +3 % causal (with a single
+// issuing thread the same split had cost bf16 3–16 %).
 //
 // Lazy rescaling: a row keeps its reference max m until a tile's max exceeds
 // it by more than kRescaleLog2 (base-2 units).  Until then P̃ = 2^(σ'S − m) is
@@ -115,7 +115,7 @@ struct FwdBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  uint64_t p_half[kQT];  // E4M3: P̃_i(j) of the first 64 keys in TMEM, O_i rescaled
+  uint64_t p_half[kQT];  // P̃_i(j) of the first 64 keys in TMEM, O_i rescaled
 };
 
 __device__ __forceinline__ unsigned int site(unsigned int s) { return (kKernFwd << 8) | s; }
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         const bool next = j + 1 < T;
         const uint32_t kb = sR + ((tv + 1) % L::kRing) * L::kSlot;
         for (int i = 0; i < kQT && ok; ++i) {
-          if (!(ok = agree(mbar_wait_inl(FP8 ? &bars->p_half[i] : &bars->p_full[i], j & 1, abort_flag, p.err, site(4)))))
+          if (!(ok = agree(mbar_wait_inl(&bars->p_half[i], j & 1, abort_flag, p.err, site(4)))))
             break;
           if (i == 0 && next && !(ok = ring_wait(tv + 1, 6))) break;
           tc_fence_after();
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           constexpr int kHalf = kBN / L::kStepK / 2;
 #pragma unroll
           for (int kk = 0; kk < kBN / L::kStepK; ++kk) {
-            if (FP8 && kk == kHalf) {  // the second half of P̃_i
+            if (kk == kHalf) {  // the second half of P̃_i
               if (!(ok = agree(mbar_wait_inl(&bars->p_full[i], j & 1, abort_flag, p.err, site(4))))) break;
               tc_fence_after();
             }
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
                 mma_bf16_ts(tmem + kColO + i * 128, tmem + i * kBN + kk * 8, bd, kIdescO, acc);
             }
           }
-          if (FP8 && !ok) break;
+          if (!ok) break;
           if (next) issue_s(i, kb);
           if (leader) mma_commit(&bars->s_full[i]);
         }
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           tmem_st16(tmem + lane_base + s_col + 16 * hf, reinterpret_cast<uint32_t(&)[16]>(w));
         else
           tmem_st32(tmem + lane_base + s_col + 32 * hf, w);
-        if (FP8 && hf == 0 && !resc) {  // E4M3: the first half goes early
+        if (hf == 0 && !resc) {  // the first half goes early
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->p_half[qt]);
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       l_run = l_run * corr + rsum;
       // O_i is stable here (its last update came before S_i(j)); rescale it in
       // TMEM only when some row of this warp moved its reference max.
-      if (FP8 ? resc : (j >= 1 && __any_sync(0xffffffffu, need))) {
+      if (resc) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       }
       tmem_wait_st();
       tc_fence_before();
-      if (FP8 && resc) mbar_arrive(&bars->p_half[qt]);
+      if (resc) mbar_arrive(&bars->p_half[qt]);
       mbar_arrive(&bars->p_full[qt]);
       m_run = m_new;
     }
