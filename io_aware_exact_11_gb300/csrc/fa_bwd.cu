@@ -353,6 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             mma_bf16_ss(tmem + kColDK, sdesc_sw128(sDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
                         sdesc_sw128(qb + kk * 2048, kTileBytes, 1024), kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
         }
+        // dK is the last reader of Q_i (dQ reads K_j and dSᵀ) and dV, long done, the
+        // last of dO_i: the producer may refill the buffer while dQ runs (measured
+        // on GB300: causal +3 %, unmasked +0.3 %).
+        if (leader) mma_commit(&bars->q_empty[it & 1]);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {  // dQ_iᵀ = K_jᵀ dSᵀ (A = K_j and B = dSᵀ, both MN-major)
           if (leader)
@@ -361,7 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         }
         if (leader) mma_commit(&bars->dq_full);
         if (leader) mma_commit(&bars->ds_free);
-        if (leader) mma_commit(&bars->q_empty[it & 1]);
       }
       if (leader) mma_commit(&bars->acc_done);
       if (*abort_flag) {
