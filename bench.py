@@ -46,7 +46,7 @@ NCU_TRAFFIC = {
     # the forward kernel at the prefill shape (B=4 H=32 N=4096 d=128), one launch
     "fwd_prefill": {"src": "2909cd273e5e5ee8", "bytes": 402746624 + 114800128},
     # the backward's main kernel at the training shape (B=2 H=16 N=8192 d=128), one launch
-    "bwd_train": {"src": "449a33ef04ebc018", "bytes": 404860160 + 222644480},
+    "bwd_train": {"src": "351b9955cd61a286", "bytes": 405801984 + 222792448},
     # the split decode kernel, captured at B=8 (H=32 N_kv=8192 d=128); its traffic is
     # proportional to B, so it is stored here scaled to the B=64 launch
     "decode_split": {"src": "5296948a01a01d33", "bytes": (1073844224 + 6728960) * 8},
