@@ -77,7 +77,8 @@ def _check(seed, B, H, Nq, Nkv, causal=False, descales=(1.0, 1.0, 1.0), sample=N
     return o
 
 
-@pytest.mark.parametrize("B,H,Nq,Nkv", [(1, 2, 256, 256), (2, 2, 300, 577), (1, 1, 129, 129)])
+@pytest.mark.parametrize("B,H,Nq,Nkv", [(1, 2, 256, 256), (2, 2, 300, 577), (1, 1, 129, 129), (2, 3, 1, 1),
+                                         (1, 2, 5, 333)])
 def test_fp8_forward_within_derived_bound(B, H, Nq, Nkv):
     _check(51, B, H, Nq, Nkv)
 

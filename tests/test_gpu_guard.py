@@ -56,14 +56,19 @@ def test_forward_writes_stay_inside_o_and_lse(B, H, Nq, Nkv, d, causal):
     _check(o, lse)
 
 
-def test_fp8_and_fp32_forward_writes_stay_inside():
+@pytest.mark.parametrize("B,H,Nq,Nkv,causal", [(1, 3, 300, 300, True), (1, 3, 300, 577, False),
+                                                (2, 1, 1, 1, False), (2, 2, 129, 700, True)])
+def test_fp8_forward_writes_stay_inside(B, H, Nq, Nkv, causal):
     import torch
-    B, H, Nq, Nkv = 1, 3, 300, 300
     q8, k8, v8 = (torch.randint(0, 120, (B, H, n, 128), dtype=torch.uint8, device="cuda") for n in (Nq, Nkv, Nkv))
     o = Guarded((B, H, Nq, 128), torch.bfloat16)
     lse = Guarded((B, H, Nq), torch.float32)
-    fa.forward_fp8(q8, k8, v8, out=o.t, lse=lse.t, causal=True)
+    fa.forward_fp8(q8, k8, v8, out=o.t, lse=lse.t, causal=causal)
     _check(o, lse)
+
+
+def test_fp32_forward_writes_stay_inside():
+    import torch
     _, dev = make_qkv(62, 1, 2, 77, 100, 64, "fp32")
     o32 = Guarded((1, 2, 77, 64), torch.float32)
     l32 = Guarded((1, 2, 77), torch.float32)
