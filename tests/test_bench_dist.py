@@ -49,3 +49,11 @@ def test_single_rank_is_identity(monkeypatch):
     monkeypatch.delenv("LOCAL_RANK", raising=False)
     assert bench.dist_env() == (1, 0, 0)
     assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_reference_arm_runs_on_rank_zero_only(capsys):
+    """Under torchrun the reference arm prints from rank 0; other ranks exit without work."""
+    import argparse
+    args = argparse.Namespace(steps=1, warmup=3)
+    assert bench.run_reference(args, 2, 1) is None
+    assert capsys.readouterr().out == ""
